@@ -1,0 +1,91 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only draws random numbers and builds the workload descriptions;
+it holds none of the attention arithmetic. Both the GPU path and the CPU
+oracle consume what it produces.
+
+Recipe (one CPU ``torch.Generator`` seeded with ``seed``):
+  Q, K, V, dO drawn in that order as ``randn(B, H, N, d)`` in fp32, then
+  rounded to bf16; for the key-padding workload the per-sequence valid key
+  lengths are drawn next as ``randint(lo, hi + 1, (B,))``. The dropout Philox
+  stream uses (seed, offset) = (0, 0). The block-sparse workload's mask is the
+  deterministic butterfly pattern built by the library itself.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool = False
+    dropout_p: float = 0.0
+    padding: tuple | None = None  # (lo, hi) inclusive range of valid key lengths
+    butterfly: bool = False
+    seed: int = 0
+    description: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# The five workloads of the benchmark suite (shapes of the pages' experiments:
+# GPT-2-medium attention, long-context LRA / Path-X lengths, block-sparse).
+TINY = Workload("tiny", 1, 1, 128, 64,
+                description="B=1 H=1 N=128 d=64, non-causal, no dropout")
+GPT2_MEDIUM = Workload("gpt2_medium", 64, 16, 1024, 64, dropout_p=0.1, padding=(512, 1024),
+                       description="B=64 H=16 N=1024 d=64, key padding U[512,1024], dropout 0.1")
+CAUSAL = Workload("causal_4k", 8, 32, 4096, 128, causal=True,
+                  description="B=8 H=32 N=4096 d=128, causal")
+LONG_D64 = Workload("long_16k_d64", 1, 16, 16384, 64,
+                    description="B=1 H=16 N=16384 d=64, non-causal")
+LONG_D128 = Workload("long_16k_d128", 1, 16, 16384, 128,
+                     description="B=1 H=16 N=16384 d=128, non-causal")
+SPARSE = Workload("butterfly_16k", 4, 16, 16384, 64, butterfly=True,
+                  description="B=4 H=16 N=16384 d=64, butterfly block mask, 128x128 blocks")
+
+ALL = {w.name: w for w in (TINY, GPT2_MEDIUM, CAUSAL, LONG_D64, LONG_D128, SPARSE)}
+
+
+def draw(w: Workload, with_grad: bool = True):
+    """Return dict with bf16 CPU tensors q, k, v, (do) and int32 seqlens (or None)."""
+    g = torch.Generator().manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    out = {}
+    names = ("q", "k", "v", "do") if with_grad else ("q", "k", "v")
+    for name in names:
+        out[name] = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    if w.padding is not None:
+        lo, hi = w.padding
+        out["seqlens"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int64).to(
+            torch.int32)
+    else:
+        out["seqlens"] = None
+    return out
+
+
+def draw_small(B, H, N, d, seed=0, with_grad=True, padding=None):
+    """Same recipe for an ad-hoc shape (parity cases and edge cases)."""
+    w = Workload("adhoc", B, H, N, d, padding=padding, seed=seed)
+    return draw(w, with_grad=with_grad)
+
+
+def sample_heads(w: Workload, count: int = 4, seed: int = 1234):
+    """Deterministic subset of (b, h) heads: first, last and seeded others."""
+    heads = [(0, 0), (w.B - 1, w.H - 1)]
+    g = torch.Generator().manual_seed(seed)
+    while len(heads) < min(count, w.B * w.H):
+        idx = int(torch.randint(0, w.B * w.H, (1,), generator=g))
+        hb = (idx // w.H, idx % w.H)
+        if hb not in heads:
+            heads.append(hb)
+    return heads

@@ -1,0 +1,204 @@
+"""CPU oracle for exact attention (fp64), with its ctypes binding.
+
+TEST INFRASTRUCTURE ONLY: the plain definition that the GPU kernels are
+checked against. Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the library itself
+never does, and it shares no code with the CUDA sources.
+
+Each function restates a definition from the pages (see ``oracle.c`` for the
+citations): standard attention ("Algorithm 0", FlashAttention deep-read report
+section 3.1) with the fused causal / key-padding / block-sparse masks and
+dropout of section 3.2, its analytic backward, Philox4x32-10 (Salmon et al.,
+SC'11) and the butterfly block mask of sections 2.6 / 3.5.
+
+Parity status: every function here is pinned by tests in ``tests/`` against
+closed forms, invariants, finite differences or an independent library
+routine, except the absolute Philox stream on a CPU-only machine, which is
+pinned on CPU only statistically and bit-exactly against cuRAND's device
+Philox4_32_10 when a GPU is present.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc + OpenMP (no fast-math)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.POINTER
+        dp = P(ctypes.c_double)
+        ip = P(ctypes.c_int)
+        u8 = P(ctypes.c_uint8)
+        u32 = P(ctypes.c_uint32)
+        lib.oracle_philox4x32_10.argtypes = [u32, u32, u32]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_p8.argtypes = [ctypes.c_double]
+        lib.oracle_p8.restype = ctypes.c_int
+        lib.oracle_butterfly.argtypes = [u8, ctypes.c_int]
+        lib.oracle_butterfly.restype = None
+        lib.oracle_dropout_keep.argtypes = [u8, ctypes.c_int, ip, ip, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64]
+        lib.oracle_dropout_keep.restype = None
+        common = [ctypes.c_int, ip, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, u8, ip]
+        lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp] + common
+        lib.oracle_fwd.restype = ctypes.c_int
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp] + common
+        lib.oracle_bwd.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _f64(a) -> np.ndarray:
+    a = np.asarray(a, dtype=np.float64)
+    return np.ascontiguousarray(a)
+
+
+def p8(p: float) -> int:
+    """Dropout threshold in 1/256 units, round(256 p)."""
+    return int(_load().oracle_p8(float(p)))
+
+
+def philox4x32_10(counter, key) -> np.ndarray:
+    """One Philox4x32-10 block: counter (4 x u32), key (2 x u32) -> 4 x u32."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c, ctypes.c_uint32), _ptr(k, ctypes.c_uint32),
+                                 _ptr(out, ctypes.c_uint32))
+    return out
+
+
+def butterfly(nb: int) -> np.ndarray:
+    """uint8 [nb, nb] butterfly block mask (r XOR c in {0} or a power of two < nb)."""
+    m = np.zeros((nb, nb), dtype=np.uint8)
+    _load().oracle_butterfly(_ptr(m, ctypes.c_uint8), int(nb))
+    return m
+
+
+def _heads(heads, B, H):
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    hb = np.ascontiguousarray(np.array([x[0] for x in heads], dtype=np.int32))
+    hh = np.ascontiguousarray(np.array([x[1] for x in heads], dtype=np.int32))
+    return heads, hb, hh
+
+
+def dropout_keep(heads, H, N, p, seed=0, offset=0) -> np.ndarray:
+    """uint8 [len(heads), N, N]: 1 where the element is kept."""
+    heads, hb, hh = _heads(heads, None, None)
+    out = np.zeros((len(heads), N, N), dtype=np.uint8)
+    _load().oracle_dropout_keep(_ptr(out, ctypes.c_uint8), len(heads), _ptr(hb, ctypes.c_int),
+                                _ptr(hh, ctypes.c_int), H, N, p8(p), seed, offset)
+    return out
+
+
+def _opt(block_mask, seqlens_k):
+    bm = None if block_mask is None else np.ascontiguousarray(np.asarray(block_mask, np.uint8))
+    sl = None if seqlens_k is None else np.ascontiguousarray(np.asarray(seqlens_k, np.int32))
+    bmp = _ptr(bm, ctypes.c_uint8) if bm is not None else ctypes.POINTER(ctypes.c_uint8)()
+    slp = _ptr(sl, ctypes.c_int) if sl is not None else ctypes.POINTER(ctypes.c_int)()
+    return bm, sl, bmp, slp
+
+
+def fwd(q, k, v, scale, causal=False, dropout_p=0.0, seed=0, offset=0, block_mask=None,
+        seqlens_k=None, heads=None, H=None):
+    """Standard attention forward in fp64.
+
+    q, k, v: [n, N, d] arrays (one entry per head listed in ``heads``, a list
+    of (b, h) pairs; default: all heads of a [B, H, N, d] tensor, in which
+    case 4-D input is accepted). Returns (o [.., N, d], lse [.., N]).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    shape4 = None
+    if q.ndim == 4:
+        B_, H_, N, d = q.shape
+        shape4 = (B_, H_)
+        heads, hb, hh = _heads(None, B_, H_)
+        H = H_
+        q, k, v = (x.reshape(B_ * H_, N, d) for x in (q, k, v))
+    else:
+        heads, hb, hh = _heads(heads, None, None)
+        N, d = q.shape[1], q.shape[2]
+    n = len(heads)
+    o = np.zeros((n, N, d), dtype=np.float64)
+    lse = np.zeros((n, N), dtype=np.float64)
+    bm, sl, bmp, slp = _opt(block_mask, seqlens_k)
+    rc = _load().oracle_fwd(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                            _ptr(v, ctypes.c_double), _ptr(o, ctypes.c_double),
+                            _ptr(lse, ctypes.c_double), n, _ptr(hb, ctypes.c_int),
+                            _ptr(hh, ctypes.c_int), int(H), N, d, float(scale), int(bool(causal)),
+                            p8(dropout_p), int(seed), int(offset), bmp, slp)
+    if rc != 0:
+        raise RuntimeError(f"oracle_fwd failed: {rc}")
+    if shape4 is not None:
+        o = o.reshape(shape4[0], shape4[1], N, d)
+        lse = lse.reshape(shape4[0], shape4[1], N)
+    return o, lse
+
+
+def bwd(q, k, v, dout, scale, causal=False, dropout_p=0.0, seed=0, offset=0, block_mask=None,
+        seqlens_k=None, heads=None, H=None):
+    """Analytic backward of L = sum(O * dO) in fp64. Returns (dq, dk, dv, D)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    shape4 = None
+    if q.ndim == 4:
+        B_, H_, N, d = q.shape
+        shape4 = (B_, H_)
+        heads, hb, hh = _heads(None, B_, H_)
+        H = H_
+        q, k, v, dout = (x.reshape(B_ * H_, N, d) for x in (q, k, v, dout))
+    else:
+        heads, hb, hh = _heads(heads, None, None)
+        N, d = q.shape[1], q.shape[2]
+    n = len(heads)
+    dq = np.zeros((n, N, d), dtype=np.float64)
+    dk = np.zeros((n, N, d), dtype=np.float64)
+    dv = np.zeros((n, N, d), dtype=np.float64)
+    D = np.zeros((n, N), dtype=np.float64)
+    bm, sl, bmp, slp = _opt(block_mask, seqlens_k)
+    rc = _load().oracle_bwd(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                            _ptr(v, ctypes.c_double), _ptr(dout, ctypes.c_double),
+                            _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                            _ptr(dv, ctypes.c_double), _ptr(D, ctypes.c_double), n,
+                            _ptr(hb, ctypes.c_int), _ptr(hh, ctypes.c_int), int(H), N, d,
+                            float(scale), int(bool(causal)), p8(dropout_p), int(seed),
+                            int(offset), bmp, slp)
+    if rc != 0:
+        raise RuntimeError(f"oracle_bwd failed: {rc}")
+    if shape4 is not None:
+        dq, dk, dv = (x.reshape(shape4[0], shape4[1], N, d) for x in (dq, dk, dv))
+        D = D.reshape(shape4[0], shape4[1], N)
+    return dq, dk, dv, D
