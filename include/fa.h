@@ -1,0 +1,137 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * The library computes exact scaled-dot-product attention the IO-aware way:
+ * the forward pass streams K/V tiles through on-chip memory, keeps a running
+ * row maximum and sum (online softmax) and writes only O and the per-row
+ * logsumexp; the backward pass recomputes S and P on chip from that
+ * logsumexp and produces dQ, dK and dV without writing any N x N matrix to
+ * device memory.  (FlashAttention deep-read report, sections 2.4 "tiling and
+ * incremental softmax", 2.5 "recomputation", 3.2 "Algorithm 1" and 3.3
+ * "backward pass and memory layout"; Attention Kernel page, "FlashAttention's
+ * insight: IO-aware" and "why tiling also works for training".)
+ *
+ * Conventions shared by every entry point
+ *   - q, k, v, o, dout, dq, dk, dv: bf16, contiguous, layout [B, H, N, d]
+ *     (row-major; element (b,h,i,c) at ((b*H + h)*N + i)*d + c). Device
+ *     pointers, 16-byte aligned. A [B, N, H, d] tensor must be transposed
+ *     by the caller first.
+ *   - lse: fp32 [B, H, N], natural-log logsumexp of the scaled scores of each
+ *     query row (this replaces the pair (m, l) that the pages store); a row
+ *     with no allowed key gets -inf and O = 0 for that row.
+ *   - d (head dimension) must be 64 or 128; N >= 1; B, H >= 1;
+ *     B*H*N < 2^31.
+ *   - scale > 0 multiplies Q K^T (the usual value is 1/sqrt(d)).
+ *   - causal != 0 masks key j for query i when j > i (square, top-left aligned).
+ *   - seqlens_k (nullable): device int32 [B]; keys j >= seqlens_k[b] are
+ *     masked for every query row of batch b (key padding; query rows are still
+ *     computed). Values are clamped to [0, N].
+ *   - block_mask (nullable): device uint8 [nb, nb], nb = ceil(N / 128), row
+ *     major, shared by all (b, h): a zero byte at (r, c) removes every pair
+ *     with query block r and key block c (FlashAttention deep-read report,
+ *     sections 2.6 and 3.5, block-sparse attention; blocks are 128 x 128).
+ *   - dropout_p in [0, 1): dropout on the normalised probabilities, applied
+ *     on chip (deep-read report section 3.2). It is quantised to
+ *     p8 = round(256 p) and the effective rate is p8/256 (see fa_dropout_p8).
+ *     Element (b,h,i,j) is dropped iff byte (j & 15) of
+ *       Philox4x32-10(counter = (j >> 4, (b*H + h)*N + i, lo32(offset), hi32(offset)),
+ *                     key = (lo32(seed), hi32(seed)))
+ *     is below p8 (byte index j&15 = word (j&15)>>2, little-endian byte j&3),
+ *     Philox as published by Salmon, Moraes, Dror and Shaw (SC'11). Kept
+ *     elements are scaled by 1/(1 - p8/256). fa_fwd and fa_bwd must be given
+ *     the same seed and offset. The logsumexp is that of the undropped softmax.
+ *   - stream: a cudaStream_t (NULL = legacy default stream). Every call is
+ *     asynchronous on that stream; the return value reports argument errors
+ *     and launch failures only.
+ *   - The library never allocates device memory. The caller owns every buffer.
+ *   - Device-side failures (a bounded wait that ran out) are recorded in a
+ *     per-device status word; fa_device_status() reads and optionally clears it.
+ */
+#ifndef FA_GB300_H_
+#define FA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/unaligned pointer, bad size, bad value */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension other than 64/128, not an sm_100-family GPU */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute) */
+  FA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than fa_bwd_workspace_size() */
+  FA_ERR_TIMEOUT = 5      /* a device-side wait ran out (reported by fa_device_status) */
+} fa_status;
+
+/* Forward pass: O = softmax(scale * Q K^T, masked) V, plus lse.
+ * Writes o [B,H,N,d] bf16 and lse [B,H,N] fp32 (both device). */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, float dropout_p, uint64_t seed,
+                 uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
+                 void* stream);
+
+/* Bytes of device workspace fa_bwd needs (the per-row D = rowsum(dO * O), fp32 [B,H,N],
+ * rounded up to 256 bytes). */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/* Backward pass of L = sum(O * dO) for the forward above. o and lse are the
+ * forward's outputs for the same inputs and options. Writes dq, dk, dv
+ * (bf16 [B,H,N,d], device). workspace: device, >= fa_bwd_workspace_size(),
+ * 16-byte aligned; its contents on entry do not matter. Three kernels run in
+ * order on `stream`: D = rowsum(dO * O); dK and dV (one pass over key tiles,
+ * recomputing S^T and P^T); dQ (one pass over query tiles, recomputing S and P).
+ * dQ is accumulated without atomics, so every output is deterministic. */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, float dropout_p, uint64_t seed, uint64_t offset,
+                 const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* Quantised dropout threshold round(256 p) used by fa_fwd / fa_bwd (-1 if p is
+ * outside [0, 1)). The effective dropout rate is fa_dropout_p8(p) / 256. */
+int fa_dropout_p8(float dropout_p);
+
+/* Test hook: writes keep[b][h][i][j] (uint8 0/1, device, [B,H,N,N]) for the
+ * dropout mask that fa_fwd / fa_bwd use with these arguments, computed by the
+ * same device Philox code. */
+fa_status fa_debug_dropout_keep(uint8_t* keep, int B, int H, int N, float dropout_p,
+                                uint64_t seed, uint64_t offset, void* stream);
+
+/* Test hook: raw Philox4x32-10 blocks from the device generator the kernels
+ * use: out[4*t .. 4*t+3] = Philox(counter[4*t .. 4*t+3], key) for t < n.
+ * counters and out are device uint32 arrays. */
+fa_status fa_debug_philox(const uint32_t* counters, uint32_t* out, int n, uint32_t key0,
+                          uint32_t key1, void* stream);
+
+/* Host helper: the butterfly block mask (FlashAttention deep-read report,
+ * sections 2.6 and 3.5, "fixed butterfly sparsity pattern"): with nb blocks per
+ * side, mask[r*nb + c] = 1 iff r XOR c is 0 or a power of two below nb.
+ * Writes nb*nb bytes to host memory. */
+fa_status fa_butterfly_mask(uint8_t* mask_host, int nb);
+
+/* Reads the status word of the current device after synchronising `stream`;
+ * returns FA_OK or the first device-side error recorded since the last clear.
+ * clear != 0 resets it to FA_OK. */
+fa_status fa_device_status(void* stream, int clear);
+
+/* Upper bound on every device-side wait, in nanoseconds (default 4e9). A wait
+ * that runs out records FA_ERR_TIMEOUT and the kernel exits early. */
+void fa_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook for failure detection: mode 1 makes the next fa_fwd launch wait on
+ * a barrier that nothing completes, so its bounded wait runs out and the
+ * kernel returns with FA_ERR_TIMEOUT recorded. The hook is consumed by that
+ * launch. mode 0 clears it. */
+void fa_test_inject_stall(int mode);
+
+/* Static description of an error code. */
+const char* fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H_ */

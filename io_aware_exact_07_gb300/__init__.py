@@ -1,0 +1,218 @@
+"""Exact IO-aware attention (forward + backward) for GB300 / sm_103a.
+
+Thin ctypes binding over the C ABI in ``include/fa.h`` (libfa_gb300.so, built
+in-tree by ``io_aware_exact_07_gb300.build``). Functions named ``fa_*`` mirror
+the C entry points one to one and only marshal arguments (torch tensors ->
+device pointers, the current torch CUDA stream); every step of the
+computation runs in the library's CUDA kernels. There is no CPU fallback: if
+the library is missing or fails to load, calls raise.
+
+``fwd`` / ``bwd`` are conveniences that allocate the outputs (and the backward
+workspace) with torch and call ``fa_fwd`` / ``fa_bwd``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_WORKSPACE = 4
+FA_ERR_TIMEOUT = 5
+
+# Symbols declared in include/fa.h.
+EXPORTS = (
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_p8", "fa_debug_dropout_keep",
+    "fa_debug_philox", "fa_butterfly_mask", "fa_device_status", "fa_set_wait_timeout_ns",
+    "fa_test_inject_stall", "fa_status_string",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def load(build_if_missing: bool = False):
+    """Load libfa_gb300.so (optionally building it first). Raises if unavailable."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing or not os.path.exists(LIB_PATH):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m io_aware_exact_07_gb300.build`")
+            from . import build as _b
+            _b.build()
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i, f, u64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64,
+                             ctypes.c_size_t)
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u64, vp, vp, vp]
+        lib.fa_fwd.restype = i
+        lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_bwd_workspace_size.restype = sz
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u64,
+                               vp, vp, vp, sz, vp]
+        lib.fa_bwd.restype = i
+        lib.fa_dropout_p8.argtypes = [f]
+        lib.fa_dropout_p8.restype = i
+        lib.fa_debug_dropout_keep.argtypes = [vp, i, i, i, f, u64, u64, vp]
+        lib.fa_debug_dropout_keep.restype = i
+        lib.fa_debug_philox.argtypes = [vp, vp, i, ctypes.c_uint32, ctypes.c_uint32, vp]
+        lib.fa_debug_philox.restype = i
+        lib.fa_butterfly_mask.argtypes = [vp, i]
+        lib.fa_butterfly_mask.restype = i
+        lib.fa_device_status.argtypes = [vp, i]
+        lib.fa_device_status.restype = i
+        lib.fa_set_wait_timeout_ns.argtypes = [u64]
+        lib.fa_set_wait_timeout_ns.restype = None
+        lib.fa_test_inject_stall.argtypes = [i]
+        lib.fa_test_inject_stall.restype = None
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def fa_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def _stream(stream=None):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _check_qkv(*ts):
+    for t in ts:
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("expected contiguous 4-D bf16 CUDA tensors [B, H, N, d]")
+
+
+def _opt_ptrs(block_mask, seqlens_k):
+    if block_mask is not None and (block_mask.dtype != torch.uint8 or not block_mask.is_cuda
+                                   or not block_mask.is_contiguous()):
+        raise ValueError("block_mask must be a contiguous uint8 CUDA tensor [nb, nb]")
+    if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda):
+        raise ValueError("seqlens_k must be an int32 CUDA tensor [B]")
+    return _ptr(block_mask), _ptr(seqlens_k)
+
+
+# ----------------------------------------------------------------- C mirrors
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal=False, dropout_p=0.0, seed=0, offset=0,
+           block_mask=None, seqlens_k=None, stream=None) -> int:
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                         int(bool(causal)), float(dropout_p), int(seed), int(offset), bm, sl,
+                         _stream(stream))
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal=False, dropout_p=0.0,
+           seed=0, offset=0, block_mask=None, seqlens_k=None, workspace=None, workspace_bytes=0,
+           stream=None) -> int:
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                         float(dropout_p), int(seed), int(offset), bm, sl, _ptr(workspace),
+                         int(workspace_bytes), _stream(stream))
+
+
+def fa_dropout_p8(p: float) -> int:
+    return int(load().fa_dropout_p8(float(p)))
+
+
+def fa_debug_dropout_keep(keep, B, H, N, dropout_p, seed=0, offset=0, stream=None) -> int:
+    return load().fa_debug_dropout_keep(_ptr(keep), B, H, N, float(dropout_p), int(seed),
+                                        int(offset), _stream(stream))
+
+
+def fa_debug_philox(counters, out, n, key0, key1, stream=None) -> int:
+    return load().fa_debug_philox(_ptr(counters), _ptr(out), int(n), int(key0), int(key1),
+                                  _stream(stream))
+
+
+def fa_butterfly_mask(nb: int) -> torch.Tensor:
+    """Host uint8 [nb, nb] butterfly block mask from the library's generator."""
+    m = torch.zeros((nb, nb), dtype=torch.uint8)
+    _check(load().fa_butterfly_mask(ctypes.c_void_p(m.data_ptr()), nb), "fa_butterfly_mask")
+    return m
+
+
+def fa_device_status(stream=None, clear=True) -> int:
+    return int(load().fa_device_status(_stream(stream), int(bool(clear))))
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    load().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_test_inject_stall(mode: int) -> None:
+    load().fa_test_inject_stall(int(mode))
+
+
+# ----------------------------------------------------------- conveniences
+
+def fwd(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0, block_mask=None,
+        seqlens_k=None, stream=None):
+    """Allocate O and lse with torch and run fa_fwd. Returns (o, lse)."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dropout_p, seed, offset, block_mask,
+                  seqlens_k, stream), "fa_fwd")
+    return o, lse
+
+
+def bwd(q, k, v, o, dout, lse, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0,
+        block_mask=None, seqlens_k=None, workspace=None, stream=None):
+    """Allocate dQ, dK, dV (and the workspace if not given) and run fa_bwd."""
+    _check_qkv(q, k, v, o, dout)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _check(fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dropout_p, seed,
+                  offset, block_mask, seqlens_k, workspace, workspace.numel(), stream), "fa_bwd")
+    return dq, dk, dv

@@ -1,0 +1,295 @@
+// C ABI of the attention library (declared in include/fa.h): argument
+// validation, TMA tensor-map encoding, kernel launches, test hooks and the
+// device status word. No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+
+namespace {
+
+// First device-side error since the last clear (one per device that loads the library).
+__device__ unsigned int g_fa_status;
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
+std::atomic<int> g_inject_stall{0};
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int major = 0;
+  unsigned int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encoder() {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  });
+  return g_encode;
+}
+
+// Per-device set-up, done once per device with that device current.
+fa_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FA_ERR_CUDA;
+    di.num_sms = prop.multiProcessorCount;
+    di.major = prop.major;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+    di.status = static_cast<unsigned int*>(p);
+    di.ready = true;
+  }
+  if (di.major != 10) return FA_ERR_UNSUPPORTED;
+  *out = &di;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int p8_of(float p) {
+  if (!(p >= 0.f) || !(p < 1.f)) return -1;
+  const int v = static_cast<int>(std::floor(static_cast<double>(p) * 256.0 + 0.5));
+  return v >= 256 ? -1 : v;
+}
+
+fa_status check_common(int B, int H, int N, int d, float scale, float dropout_p) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (p8_of(dropout_p) < 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// [B*H, N, d] bf16 tensor, boxes of 64 columns x 128 rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+bool encode_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+fa::MaskParams make_mask(int B, int H, int N, int causal, const uint8_t* bm, const int32_t* sl) {
+  fa::MaskParams m;
+  m.B = B;
+  m.H = H;
+  m.N = N;
+  m.nb = (N + fa::kTile - 1) / fa::kTile;
+  m.causal = causal ? 1 : 0;
+  m.block_mask = bm;
+  m.seqlens_k = sl;
+  return m;
+}
+
+fa::DropParams make_drop(float p, uint64_t seed, uint64_t offset) {
+  fa::DropParams d;
+  d.p8 = p8_of(p);
+  d.keep_scale = static_cast<float>(1.0 / (1.0 - d.p8 / 256.0));
+  d.seed_lo = static_cast<uint32_t>(seed);
+  d.seed_hi = static_cast<uint32_t>(seed >> 32);
+  d.off_lo = static_cast<uint32_t>(offset);
+  d.off_hi = static_cast<uint32_t>(offset >> 32);
+  return d;
+}
+
+fa::SyncParams make_sync(const DeviceInfo* di, bool consume_stall) {
+  fa::SyncParams s;
+  s.status = di->status;
+  s.timeout_ns = g_timeout_ns.load();
+  s.inject_stall = consume_stall ? g_inject_stall.exchange(0) : 0;
+  return s;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, float dropout_p, uint64_t seed,
+                 uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
+                 void* stream) {
+  fa_status st = check_common(B, H, N, d, scale, dropout_p);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if (!encode_map(&tq, q, B * H, N, d) || !encode_map(&tk, k, B * H, N, d) ||
+      !encode_map(&tv, v, B * H, N, d))
+    return FA_ERR_CUDA;
+  fa::FwdArgs a;
+  a.mask = make_mask(B, H, N, causal, block_mask, seqlens_k);
+  a.drop = make_drop(dropout_p, seed, offset);
+  a.sync = make_sync(di, true);
+  a.scale_log2 = scale * fa::kLog2e;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  cudaError_t e = fa::launch_fwd(tq, tk, tv, a, d, a.drop.p8 > 0, di->num_sms,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  (void)d;
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return round256(static_cast<size_t>(B) * H * N * sizeof(float));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, float dropout_p, uint64_t seed, uint64_t offset,
+                 const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  fa_status st = check_common(B, H, N, d, scale, dropout_p);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < fa_bwd_workspace_size(B, H, N, d) ||
+      !aligned16(workspace))
+    return FA_ERR_WORKSPACE;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_map(&tq, q, B * H, N, d) || !encode_map(&tk, k, B * H, N, d) ||
+      !encode_map(&tv, v, B * H, N, d) || !encode_map(&tdo, dout, B * H, N, d))
+    return FA_ERR_CUDA;
+  fa::BwdArgs a;
+  a.mask = make_mask(B, H, N, causal, block_mask, seqlens_k);
+  a.drop = make_drop(dropout_p, seed, offset);
+  a.sync = make_sync(di, false);
+  a.scale = scale;
+  a.scale_log2 = scale * fa::kLog2e;
+  a.o = static_cast<const __nv_bfloat16*>(o);
+  a.dout = static_cast<const __nv_bfloat16*>(dout);
+  a.lse = lse;
+  a.dsum = static_cast<float*>(workspace);
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool drop = a.drop.p8 > 0;
+  cudaError_t e = fa::launch_bwd_preprocess(a, d, di->num_sms, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_dkdv(tq, tk, tv, tdo, a, d, drop, di->num_sms, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_dq(tq, tk, tv, tdo, a, d, drop, di->num_sms, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_dropout_p8(float dropout_p) { return p8_of(dropout_p); }
+
+fa_status fa_debug_dropout_keep(uint8_t* keep, int B, int H, int N, float dropout_p,
+                                uint64_t seed, uint64_t offset, void* stream) {
+  if (keep == nullptr || B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (p8_of(dropout_p) < 0) return FA_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  fa_status st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = fa::launch_debug_dropout(keep, B, H, N, make_drop(dropout_p, seed, offset),
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_debug_philox(const uint32_t* counters, uint32_t* out, int n, uint32_t key0,
+                          uint32_t key1, void* stream) {
+  if (counters == nullptr || out == nullptr || n < 0) return FA_ERR_INVALID_ARG;
+  if (!aligned16(counters) || !aligned16(out)) return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  DeviceInfo* di = nullptr;
+  fa_status st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e =
+      fa::launch_debug_philox(counters, out, n, key0, key1, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_butterfly_mask(uint8_t* mask_host, int nb) {
+  if (mask_host == nullptr || nb < 1 || nb > 65536) return FA_ERR_INVALID_ARG;
+  // Partner of block r at stride 2^k is r XOR 2^k; the diagonal is stride 0.
+  for (int r = 0; r < nb; ++r) {
+    for (int c = 0; c < nb; ++c) {
+      const unsigned x = static_cast<unsigned>(r ^ c);
+      mask_host[static_cast<size_t>(r) * nb + c] =
+          static_cast<uint8_t>(x == 0u || (x & (x - 1u)) == 0u);
+    }
+  }
+  return FA_OK;
+}
+
+fa_status fa_device_status(void* stream, int clear) {
+  DeviceInfo* di = nullptr;
+  fa_status st = device_info(&di);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, di->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  return static_cast<fa_status>(v);
+}
+
+void fa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+void fa_test_inject_stall(int mode) { g_inject_stall.store(mode ? 1 : 0); }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or device";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

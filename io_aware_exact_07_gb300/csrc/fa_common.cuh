@@ -1,0 +1,122 @@
+// Shared device-side pieces of the attention kernels: launch parameters,
+// tile validity (causal / key padding / block-sparse), the Philox dropout
+// generator and the device status word.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kTile = 128;               // query / key tile edge (rows), and block-mask granularity
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device status codes (mirror fa_status in include/fa.h).
+constexpr unsigned kStatusTimeout = 5u;
+
+struct MaskParams {
+  int B, H, N;
+  int nb;                       // ceil(N / 128): tiles per side, block-mask row length
+  int causal;
+  const uint8_t* block_mask;    // [nb, nb] or null
+  const int32_t* seqlens_k;     // [B] or null
+};
+
+struct DropParams {
+  int p8;                       // drop iff Philox byte < p8
+  float keep_scale;             // 1 / (1 - p8 / 256)
+  uint32_t seed_lo, seed_hi, off_lo, off_hi;
+};
+
+struct SyncParams {
+  unsigned int* status;         // device status word (first error wins)
+  unsigned long long timeout_ns;
+  int inject_stall;             // test hook: wait on a barrier that never completes
+};
+
+__device__ __forceinline__ void record_error(unsigned int* status, unsigned code) {
+  atomicCAS(status, 0u, code);
+}
+
+// Number of valid keys of batch b (key padding clamps to [0, N]).
+__device__ __forceinline__ int kv_len_of(const MaskParams& m, int b) {
+  if (m.seqlens_k == nullptr) return m.N;
+  int L = m.seqlens_k[b];
+  return L < 0 ? 0 : (L > m.N ? m.N : L);
+}
+
+// Whether the (query tile qt, key tile kt) pair has any allowed element.
+// n_kv = ceil(kv_len / 128), n_q = ceil(N / 128).
+__device__ __forceinline__ bool tile_valid(const MaskParams& m, int qt, int kt, int n_q,
+                                           int n_kv) {
+  if (qt >= n_q || kt >= n_kv) return false;
+  if (m.causal && kt > qt) return false;
+  if (m.block_mask != nullptr && m.block_mask[qt * m.nb + kt] == 0) return false;
+  return true;
+}
+
+// Whether the pair needs a per-element mask (causal diagonal, or key tile
+// crossing kv_len). Query rows beyond N are never written, so the query tail
+// needs none.
+__device__ __forceinline__ bool tile_needs_element_mask(const MaskParams& m, int qt, int kt,
+                                                        int kv_len) {
+  return (m.causal && kt == qt) || ((kt + 1) * kTile > kv_len);
+}
+
+// Bits j in [32*c, 32*c + 32) that are valid for query tile qt, computed by a
+// whole warp (one candidate per lane).
+__device__ __forceinline__ uint32_t warp_valid_bits(const MaskParams& m, int qt, int chunk,
+                                                    int n_q, int n_kv) {
+  const int lane = threadIdx.x & 31;
+  const bool v = tile_valid(m, qt, chunk * 32 + lane, n_q, n_kv);
+  return __ballot_sync(0xffffffffu, v);
+}
+
+// Same, transposed: query tiles qt in [32*c, 32*c + 32) valid for key tile kt.
+__device__ __forceinline__ uint32_t warp_valid_bits_t(const MaskParams& m, int kt, int chunk,
+                                                      int n_q, int n_kv) {
+  const int lane = threadIdx.x & 31;
+  const bool v = tile_valid(m, chunk * 32 + lane, kt, n_q, n_kv);
+  return __ballot_sync(0xffffffffu, v);
+}
+
+// ------------------------------------------------------------------ Philox
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+// as 1, 2, 3", SC'11): ten rounds of two 32x32 -> 64-bit multiplies by the
+// round multipliers, the high halves xored with the other counter words and
+// the key, with the key advanced by the Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Keep masks for the 16 keys [16*g, 16*g + 16) of query row `row_global`
+// ((b*H + h)*N + i): each byte is 0xFF where the element is kept, 0 where dropped.
+__device__ __forceinline__ uint4 dropout_keep16(const DropParams& d, uint32_t row_global,
+                                                uint32_t key_group) {
+  const uint4 r = philox4x32_10(make_uint4(key_group, row_global, d.off_lo, d.off_hi), d.seed_lo,
+                                d.seed_hi);
+  const uint32_t thr = static_cast<uint32_t>(d.p8) * 0x01010101u;
+  // per-byte unsigned compare: 0xFF where byte >= p8
+  return make_uint4(__vcmpgeu4(r.x, thr), __vcmpgeu4(r.y, thr), __vcmpgeu4(r.z, thr),
+                    __vcmpgeu4(r.w, thr));
+}
+
+// bf16x2 helpers for the epilogues.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) { return pack_bf16x2(lo, hi); }
+
+}  // namespace fa

@@ -1,0 +1,48 @@
+"""Shared helpers for the GPU-vs-oracle parity tests (inputs, tolerances)."""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from io_aware_exact_07_gb300 import inputs
+
+# Accuracy bars for bf16 inputs with fp32 accumulation: O max-abs, lse max-abs,
+# and relative Frobenius error of dQ, dK, dV.
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+GRAD_RTOL = 2e-2
+
+
+def make_case(B, H, N, d, seed=0, padding=None, with_grad=True):
+    return inputs.draw_small(B, H, N, d, seed=seed, with_grad=with_grad, padding=padding)
+
+
+def to_dev(x):
+    return None if x is None else x.cuda()
+
+
+def oracle_heads(x, heads):
+    """Slice [B, H, N, d] bf16 tensor to fp64 [len(heads), N, d] for the given (b, h)."""
+    return np.stack([x[b, h].double().numpy() for b, h in heads])
+
+
+def rel_fro(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    nb = np.linalg.norm(b)
+    return np.linalg.norm(a - b) / (nb if nb > 0 else 1.0)
+
+
+def lse_err(gpu, ref):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    both_inf = np.isneginf(gpu) & np.isneginf(ref)
+    diff = np.where(both_inf, 0.0, np.abs(gpu - ref))
+    return float(np.max(diff)) if diff.size else 0.0
+
+
+def butterfly_dev(N):
+    from io_aware_exact_07_gb300 import fa_butterfly_mask
+    nb = math.ceil(N / 128)
+    return fa_butterfly_mask(nb).cuda()
