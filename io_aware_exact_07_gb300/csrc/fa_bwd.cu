@@ -1,6 +1,1160 @@
+// Backward pass of exact attention on sm_103a. Nothing of size N x N is
+// stored: S and P are recomputed on chip from Q, K and the saved logsumexp
+// (FlashAttention deep-read report, sections 2.5 "recomputation" and 3.3
+// "backward pass and memory layout"; Attention Kernel page, "why tiling also
+// works for training"). With L = sum(O * dO):
+//   D_i   = sum_c dO_ic O_ic                       (preprocess kernel)
+//   P_ij  = exp(scale q_i.k_j - lse_i), masked; Z_ij the dropout keep bit
+//   dV_j  = sum_i P_ij Z_ij/(1-p) dO_i
+//   dS_ij = P_ij (Z_ij/(1-p) dO_i.v_j - D_i)
+//   dK_j  = scale sum_i dS_ij q_i                  (key-tile kernel: dK, dV)
+//   dQ_i  = scale sum_j dS_ij k_j                  (query-tile kernel: dQ)
+// The five contractions of the backward (the cross-paper synthesis page notes
+// the backward's five matmuls against the forward's two) are split over two
+// kernels so that every output tile is owned by exactly one CTA: dQ needs no
+// atomics and every result is deterministic. The price is that S and dP are
+// computed twice (seven tensor-core contractions instead of five).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_common.cuh"
 #include "fa_kernels.h"
+
 namespace fa {
-cudaError_t launch_bwd_preprocess(const BwdArgs&, int, int, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_bwd_dkdv(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const BwdArgs&, int, bool, int, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_bwd_dq(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const BwdArgs&, int, bool, int, cudaStream_t) { return cudaErrorNotSupported; }
+
+namespace {
+
+constexpr int kBwdThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+
+// ------------------------------------------------------------------ preprocess
+// D = rowsum(dO * O) in fp32; 8 threads per row, 16-byte loads.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                                             const __nv_bfloat16* __restrict__ dout,
+                                                             float* __restrict__ dsum,
+                                                             long long rows) {
+  const int sub = threadIdx.x & 7;
+  const unsigned gmask = 0xFFu << (threadIdx.x & 24);
+  const long long groups_per_grid = (static_cast<long long>(gridDim.x) * blockDim.x) >> 3;
+  for (long long row = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 3;
+       row < rows; row += groups_per_grid) {
+    float acc = 0.f;
+#pragma unroll
+    for (int c = sub; c < D / 8; c += 8) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + c);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + c);
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[e]));
+        const float2 fb2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[e]));
+        acc = fmaf(fa2.x, fb2.x, acc);
+        acc = fmaf(fa2.y, fb2.y, acc);
+      }
+    }
+    acc += __shfl_xor_sync(gmask, acc, 4, 8);
+    acc += __shfl_xor_sync(gmask, acc, 2, 8);
+    acc += __shfl_xor_sync(gmask, acc, 1, 8);
+    if (sub == 0) dsum[row] = acc;
+  }
 }
+
+// lse in log2 units for recomputing P = exp2(s * scale * log2e - lse2); rows
+// outside [0, N) and rows without any allowed key map to +inf, so P = 0.
+__device__ __forceinline__ float lse2_of(const float* lse, long long idx, bool in_range) {
+  if (!in_range) return INFINITY;
+  const float l = lse[idx];
+  return (l == -INFINITY) ? INFINITY : l * kLog2e;
+}
+
+// ================================================================== dK, dV
+// One work unit = one (b, h) head and one 128-row key tile (K_j, V_j stay in
+// shared memory); the loop runs over the query tiles that may attend to it.
+//   warp 8      TMA producer: K_j, V_j per unit; Q_i, dO_i (and lse_i, D_i via
+//               plain loads) through an NS-stage ring.
+//   warp 9      MMA issuer: S^T = K Q^T, dP^T = V dO^T (shared-memory
+//               operands), dV += P^T dO and dK += dS^T Q (A from tensor memory).
+//   warps 0-7   two warpgroups, each owning 64 of the 128 query columns of
+//               every tile (thread = key row): P^T = exp2(S^T c - lse2),
+//               dropout, dS^T = P^T (Z dP^T / (1-p) - D); P^T and dS^T go back
+//               to tensor memory as bf16 over the columns they were read from.
+// Tensor memory: dV [0, d), dK [d, 2d), S^T [2d, 2d+128), dP^T [2d+128, 2d+256).
+template <int D>
+struct DkdvLayout {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;
+  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
+  static constexpr int kLseOff = kDOOff + kStages * kTileBytes;      // kStages x 128 fp32
+  static constexpr int kDsumOff = kLseOff + kStages * 512;          // kStages x 128 fp32
+  static constexpr int kDropOff = kDsumOff + kStages * 512;         // 8 warps x 2 KB Philox scratch
+  static constexpr int kBarOff = kDropOff + 8 * 2048;
+  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+  __device__ static constexpr uint32_t col_dv() { return 0u; }
+  __device__ static constexpr uint32_t col_dk() { return static_cast<uint32_t>(D); }
+  __device__ static constexpr uint32_t col_st() { return static_cast<uint32_t>(2 * D); }
+  __device__ static constexpr uint32_t col_dpt() { return static_cast<uint32_t>(2 * D + 128); }
+};
+
+template <int D, bool DROPOUT>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
+  using L = DkdvLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const MaskParams& mk = args.mask;
+  const int N = mk.N;
+  const int BH = mk.B * mk.H;
+  const int n_t = (N + kTile - 1) / kTile;  // query tiles == key tiles
+  const int n_units = BH * n_t;
+
+  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff + 8);
+  float* lse_s = reinterpret_cast<float*>(smem + L::kLseOff);
+  float* dsum_s = reinterpret_cast<float*>(smem + L::kDsumOff);
+
+  uint32_t b_kv_full, b_kv_empty, b_q_full[4], b_q_empty[4], b_st_full, b_dpt_full, b_p_ready,
+      b_ds_ready, b_acc_full, b_acc_free, b_drain;
+  {
+    int i = 0;
+    auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
+    b_kv_full = nb();
+    b_kv_empty = nb();
+    for (int s = 0; s < L::kStages; ++s) b_q_full[s] = nb();
+    for (int s = 0; s < L::kStages; ++s) b_q_empty[s] = nb();
+    b_st_full = nb();
+    b_dpt_full = nb();
+    b_p_ready = nb();
+    b_ds_ready = nb();
+    b_acc_full = nb();
+    b_acc_free = nb();
+    b_drain = nb();
+  }
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(b_kv_full, 1);
+    mbar_init(b_kv_empty, 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(b_q_full[s], 32);
+      mbar_init(b_q_empty[s], 1 + 8);
+    }
+    mbar_init(b_st_full, 1);
+    mbar_init(b_dpt_full, 1);
+    mbar_init(b_p_ready, 256);
+    mbar_init(b_ds_ready, 256);
+    mbar_init(b_acc_full, 1);
+    mbar_init(b_acc_free, 256);
+    mbar_init(b_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t tmo = args.sync.timeout_ns;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    record_error(args.sync.status, kStatusTimeout);
+  };
+  const uint32_t sK = smem_u32(smem + L::kKOff);
+  const uint32_t sV = smem_u32(smem + L::kVOff);
+  const uint32_t sQ = smem_u32(smem + L::kQOff);
+  const uint32_t sDO = smem_u32(smem + L::kDOOff);
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0, kv_arms = 0, q_arms = 0;
+    bool ok = true;
+    int unit_count = 0;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+      const int bh = u / n_t, kt = u % n_t;
+      const int b = bh / mk.H;
+      const int kv_len = kv_len_of(mk, b);
+      const int n_kv = (kv_len + kTile - 1) / kTile;
+      if (unit_count > 0 && !mbar_wait_warp(b_kv_empty, (unit_count - 1) & 1, tmo, abort_flag)) {
+        fail();
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        mbar_expect_tx(b_kv_full, 2 * L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_3d(sK + c * 16384, &tm_k, c * 64, kt * kTile, bh, b_kv_full);
+          tma_load_3d(sV + c * 16384, &tm_v, c * 64, kt * kTile, bh, b_kv_full);
+        }
+      }
+      ++kv_arms;
+      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+        uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+        while (bits != 0u) {
+          const int qt = chunk * 32 + (__ffs(bits) - 1);
+          bits &= bits - 1;
+          const int s = it % L::kStages;
+          const uint32_t ph = (it / L::kStages) & 1u;
+          if (!mbar_wait_warp(b_q_empty[s], ph ^ 1u, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          // lse (log2 units) and D of the 128 query rows of this tile
+          float4 l4, d4;
+          float* lp = &l4.x;
+          float* dp = &d4.x;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int row = qt * kTile + 4 * lane + r;
+            const bool in = row < N;
+            const long long idx = static_cast<long long>(bh) * N + row;
+            lp[r] = lse2_of(args.lse, idx, in);
+            dp[r] = in ? args.dsum[idx] : 0.f;
+          }
+          reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
+          reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
+          if (lane == 0) {
+            mbar_expect_tx(b_q_full[s], 2 * L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c) {
+              tma_load_3d(sQ + s * L::kTileBytes + c * 16384, &tm_q, c * 64, qt * kTile, bh,
+                          b_q_full[s]);
+              tma_load_3d(sDO + s * L::kTileBytes + c * 16384, &tm_do, c * 64, qt * kTile, bh,
+                          b_q_full[s]);
+            }
+          } else {
+            mbar_arrive(b_q_full[s]);
+          }
+          ++q_arms;
+          ++it;
+        }
+      }
+    }
+    if (kv_arms) mbar_wait_warp(b_kv_full, (kv_arms - 1) & 1, tmo, nullptr);
+#pragma unroll
+    for (int s = 0; s < L::kStages; ++s)
+      if (q_arms > static_cast<uint32_t>(s))
+        mbar_wait_warp(b_q_full[s], ((q_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);
+    const bool elected = lane == 0;
+    uint32_t it = 0, p_cnt = 0, ds_cnt = 0;
+    bool ok = true;
+    int unit_count = 0;
+    // acc (+)= A[tmem, 64-column halves at a0 and a0 + 64] * B[smem, MN-major]
+    auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base, bool accumulate) {
+      const uint64_t db = sdesc_sw128(b_base, 16384, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a = tmem + a_col + (kk >> 2) * 64 + (kk & 3) * 8;
+        mma_ts(tmem + d_col, a, db + static_cast<uint64_t>((kk * 2048) >> 4), kIdAcc,
+               (accumulate || kk > 0) ? 1u : 0u);
+      }
+    };
+    auto issue_ss = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+      const uint64_t da = sdesc_sw128(a_base, 16, 1024);
+      const uint64_t db = sdesc_sw128(b_base, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_ss(tmem + d_col, da + (off >> 4), db + (off >> 4), kIdS, kk > 0 ? 1u : 0u);
+      }
+    };
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+      const int bh = u / n_t, kt = u % n_t;
+      const int b = bh / mk.H;
+      const int kv_len = kv_len_of(mk, b);
+      const int n_kv = (kv_len + kTile - 1) / kTile;
+      (void)bh;
+      if (!mbar_wait_warp(b_kv_full, unit_count & 1, tmo, abort_flag)) {
+        fail();
+        ok = false;
+        break;
+      }
+      int t = 0;
+      int prev_s = -1;
+      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+        uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+        while (bits != 0u) {
+          bits &= bits - 1;
+          const int s = it % L::kStages;
+          const uint32_t ph = (it / L::kStages) & 1u;
+          if (!mbar_wait_warp(b_q_full[s], ph, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elected) {
+            issue_ss(L::col_st(), sK, sQ + s * L::kTileBytes);  // S^T = K Q^T
+            mma_commit(b_st_full);
+          }
+          __syncwarp();
+          if (t > 0) {  // dK += dS^T(prev) Q(prev)
+            if (!mbar_wait_warp(b_ds_ready, ds_cnt & 1, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            ++ds_cnt;
+            tc_fence_after();
+            if (elected) {
+              issue_acc(L::col_dk(), L::col_dpt(), sQ + prev_s * L::kTileBytes, t - 1 > 0);
+              mma_commit(b_q_empty[prev_s]);
+            }
+            __syncwarp();
+          }
+          if (elected) {
+            issue_ss(L::col_dpt(), sV, sDO + s * L::kTileBytes);  // dP^T = V dO^T
+            mma_commit(b_dpt_full);
+          }
+          __syncwarp();
+          if (!mbar_wait_warp(b_p_ready, p_cnt & 1, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          ++p_cnt;
+          if (t == 0 && unit_count > 0 &&
+              !mbar_wait_warp(b_acc_free, (unit_count - 1) & 1, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elected) issue_acc(L::col_dv(), L::col_st(), sDO + s * L::kTileBytes, t > 0);
+          __syncwarp();
+          prev_s = s;
+          ++t;
+          ++it;
+        }
+      }
+      if (!ok) break;
+      if (t > 0) {
+        if (!mbar_wait_warp(b_ds_ready, ds_cnt & 1, tmo, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        ++ds_cnt;
+        tc_fence_after();
+        if (elected) {
+          issue_acc(L::col_dk(), L::col_dpt(), sQ + prev_s * L::kTileBytes, t - 1 > 0);
+          mma_commit(b_q_empty[prev_s]);
+        }
+        __syncwarp();
+      } else if (unit_count > 0) {
+        if (!mbar_wait_warp(b_acc_free, (unit_count - 1) & 1, tmo, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+      }
+      if (elected) {
+        mma_commit(b_acc_full);
+        mma_commit(b_kv_empty);
+      }
+      __syncwarp();
+    }
+    if (elected) mma_commit(b_drain);
+    __syncwarp();
+    mbar_wait_warp(b_drain, 0, tmo, nullptr);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int wg = warp >> 2;   // query columns [64 wg, 64 wg + 64)
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // key row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tSt = tmem + lane_base + L::col_st() + 64 * wg;
+    const uint32_t tDPt = tmem + lane_base + L::col_dpt() + 64 * wg;
+    const float c_log2 = args.scale_log2;
+    uint32_t* drop_scratch = reinterpret_cast<uint32_t*>(smem + L::kDropOff + warp * 2048);
+    uint32_t it = 0, st_cnt = 0, dpt_cnt = 0;
+    bool ok = true;
+    int unit_count = 0;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+      const int bh = u / n_t, kt = u % n_t;
+      const int b = bh / mk.H;
+      const int kv_len = kv_len_of(mk, b);
+      const int n_kv = (kv_len + kTile - 1) / kTile;
+      const int key = kt * kTile + r;
+      int n_done = 0;
+      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+        uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+        while (bits != 0u) {
+          const int qt = chunk * 32 + (__ffs(bits) - 1);
+          bits &= bits - 1;
+          const int s = it % L::kStages;
+          const float* lse_t = lse_s + s * 128 + 64 * wg;
+          const float* dsum_t = dsum_s + s * 128 + 64 * wg;
+          const int q0 = qt * kTile + 64 * wg;  // first query column of this thread's half
+          // Dropout keep bits of this (key, 64 queries) strip.
+          uint32_t zb0 = 0xFFFFFFFFu, zb1 = 0xFFFFFFFFu;
+          if constexpr (DROPOUT) {
+            const uint32_t key0 = static_cast<uint32_t>(kt * kTile + quad * 32);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int idx = lane + 32 * m;
+              const int c = idx >> 1, gs = idx & 1;
+              const uint32_t rowg = static_cast<uint32_t>(bh) * static_cast<uint32_t>(N) +
+                                    static_cast<uint32_t>(q0 + c);
+              const uint4 kw = dropout_keep16(args.drop, rowg, (key0 >> 4) + gs);
+              reinterpret_cast<uint4*>(drop_scratch)[c * 2 + gs] = kw;
+            }
+            __syncwarp();
+            zb0 = 0u;
+            zb1 = 0u;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const uint32_t w = drop_scratch[(c * 2 + (lane >> 4)) * 4 + ((lane & 15) >> 2)];
+              const uint32_t kbit = (w >> (8 * (lane & 3))) & 1u;  // bytes are 0x00 or 0xFF
+              if (c < 32) zb0 |= kbit << c;
+              else zb1 |= kbit << (c - 32);
+            }
+            __syncwarp();
+          }
+          // ---- phase 1: P^T
+          if (!mbar_wait_warp(b_st_full, st_cnt & 1, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          ++st_cnt;
+          tc_fence_after();
+          float p[64];
+          {
+            uint32_t sr[64];
+            tmem_ld32(tSt, &sr[0]);
+            tmem_ld32(tSt + 32, &sr[32]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4) {
+              const float4 l4 = reinterpret_cast<const float4*>(lse_t)[c4];
+              p[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 0]), c_log2, -l4.x));
+              p[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 1]), c_log2, -l4.y));
+              p[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 2]), c_log2, -l4.z));
+              p[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 3]), c_log2, -l4.w));
+            }
+          }
+          if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
+            const bool key_ok = key < kv_len;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const bool allowed = key_ok && (!mk.causal || key <= q0 + c);
+              p[c] = allowed ? p[c] : 0.f;
+            }
+          }
+          {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              float a0 = p[2 * c], a1 = p[2 * c + 1];
+              if constexpr (DROPOUT) {
+                const uint32_t zw = (c < 16) ? zb0 : zb1;
+                const int sh = (2 * c) & 31;
+                a0 = ((zw >> sh) & 1u) ? a0 : 0.f;
+                a1 = ((zw >> (sh + 1)) & 1u) ? a1 : 0.f;
+              }
+              pk[c] = pack_bf16x2(a0, a1);
+            }
+            tmem_st32(tSt, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(b_p_ready);
+          // ---- phase 2: dS^T
+          if (!mbar_wait_warp(b_dpt_full, dpt_cnt & 1, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          ++dpt_cnt;
+          tc_fence_after();
+          {
+            uint32_t pk[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t dr[32];
+              tmem_ld32(tDPt + 32 * h, dr);
+              tmem_ld_wait();
+#pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 d4 = reinterpret_cast<const float4*>(dsum_t)[8 * h + c4];
+                const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                float ds[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int c = 32 * h + 4 * c4 + e;
+                  float z = args.drop.keep_scale;
+                  if constexpr (DROPOUT) {
+                    const uint32_t zw = (c < 32) ? zb0 : zb1;
+                    z = ((zw >> (c & 31)) & 1u) ? z : 0.f;
+                  }
+                  ds[e] = p[c] * fmaf(z, __uint_as_float(dr[4 * c4 + e]), -dv4[e]);
+                }
+                pk[16 * h + 2 * c4] = pack_bf16x2(ds[0], ds[1]);
+                pk[16 * h + 2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+              }
+            }
+            tmem_st32(tDPt, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(b_ds_ready);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_q_empty[s]);  // lse / D of this stage no longer read
+          ++n_done;
+          ++it;
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK
+      if (!mbar_wait_warp(b_acc_full, unit_count & 1, tmo, abort_flag)) {
+        fail();
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tAcc = tmem + lane_base + (wg == 0 ? L::col_dv() : L::col_dk());
+      const float mult = (wg == 0) ? args.drop.keep_scale : args.scale;
+      __nv_bfloat16* dst_base = (wg == 0) ? args.dv : args.dk;
+      __nv_bfloat16* dst = dst_base + (static_cast<size_t>(bh) * N + static_cast<size_t>(key)) * D;
+      const bool row_ok = key < N;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        if (n_done > 0) {
+          tmem_ld32(tAcc + 32 * c, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          pk[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mult, __uint_as_float(v[2 * k + 1]) * mult);
+        if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(b_acc_free);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================== dQ
+// One work unit = one (b, h) head and 256 query rows (query tiles a and b);
+// the loop runs over the key tiles either tile attends to.
+//   warp 8      TMA producer: Q_a, Q_b, dO_a, dO_b per unit; K_j and V_j through
+//               separate rings (K is still needed for dQ after V is done).
+//   warp 9      MMA issuer: S_x = Q_x K^T, dP_x = dO_x V^T (shared-memory
+//               operands) and dQ_x += dS_x K (A from tensor memory).
+//   warps 0-7   one warpgroup per query tile (thread = query row): P = exp2(S c -
+//               lse2) kept packed as bf16 in registers while dP overwrites S in
+//               tensor memory; then dS = P (Z dP/(1-p) - D) written over dP.
+// Tensor memory: S/dP/dS of tile x at [128 x, 128 x + 128); dQ_x at 256 + x d.
+template <int D>
+struct DqLayout {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kKStages = (D == 64) ? 4 : 2;
+  static constexpr int kVStages = (D == 64) ? 2 : 1;
+  static constexpr int kQOff = 0;                       // Q_a, Q_b
+  static constexpr int kDOOff = 2 * kTileBytes;         // dO_a, dO_b
+  static constexpr int kKOff = 4 * kTileBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kNumBars = 3 + 2 * kKStages + 2 * kVStages + 12 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+  __device__ static constexpr uint32_t col_sp(int x) { return static_cast<uint32_t>(x) * 128u; }
+  __device__ static constexpr uint32_t col_dq(int x) { return 256u + static_cast<uint32_t>(x * D); }
+};
+
+template <int D, bool DROPOUT>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
+  using L = DqLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const MaskParams& mk = args.mask;
+  const int N = mk.N;
+  const int BH = mk.B * mk.H;
+  const int n_q = (N + kTile - 1) / kTile;
+  const int n_qblk = (n_q + 1) / 2;
+  const int n_units = BH * n_qblk;
+
+  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff + 8);
+
+  uint32_t b_q_full[2], b_q_empty, b_k_full[4], b_k_empty[4], b_v_full[2], b_v_empty[2];
+  uint32_t b_s_full[2], b_sp_free[2], b_dp_full[2], b_ds_ready[2], b_dq_full[2], b_dq_free[2];
+  uint32_t b_drain;
+  {
+    int i = 0;
+    auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
+    b_q_full[0] = nb();
+    b_q_full[1] = nb();
+    b_q_empty = nb();
+    for (int s = 0; s < L::kKStages; ++s) b_k_full[s] = nb();
+    for (int s = 0; s < L::kKStages; ++s) b_k_empty[s] = nb();
+    for (int s = 0; s < L::kVStages; ++s) b_v_full[s] = nb();
+    for (int s = 0; s < L::kVStages; ++s) b_v_empty[s] = nb();
+    for (int x = 0; x < 2; ++x) {
+      b_s_full[x] = nb();
+      b_sp_free[x] = nb();
+      b_dp_full[x] = nb();
+      b_ds_ready[x] = nb();
+      b_dq_full[x] = nb();
+      b_dq_free[x] = nb();
+    }
+    b_drain = nb();
+  }
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(b_q_full[0], 1);
+    mbar_init(b_q_full[1], 1);
+    mbar_init(b_q_empty, 1);
+    for (int s = 0; s < L::kKStages; ++s) {
+      mbar_init(b_k_full[s], 1);
+      mbar_init(b_k_empty[s], 1);
+    }
+    for (int s = 0; s < L::kVStages; ++s) {
+      mbar_init(b_v_full[s], 1);
+      mbar_init(b_v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(b_s_full[x], 1);
+      mbar_init(b_sp_free[x], 128);
+      mbar_init(b_dp_full[x], 1);
+      mbar_init(b_ds_ready[x], 128);
+      mbar_init(b_dq_full[x], 1);
+      mbar_init(b_dq_free[x], 128);
+    }
+    mbar_init(b_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t tmo = args.sync.timeout_ns;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    record_error(args.sync.status, kStatusTimeout);
+  };
+  const uint32_t sQ = smem_u32(smem + L::kQOff);
+  const uint32_t sDO = smem_u32(smem + L::kDOOff);
+  const uint32_t sK = smem_u32(smem + L::kKOff);
+  const uint32_t sV = smem_u32(smem + L::kVOff);
+
+  auto unit_coords = [&](int u, int& bh, int& b, int& qt0) {
+    bh = u / n_qblk;
+    int qb = u % n_qblk;
+    if (mk.causal) qb = n_qblk - 1 - qb;
+    b = bh / mk.H;
+    qt0 = 2 * qb;
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0, k_arms = 0, v_arms = 0, q_arms = 0;
+    bool ok = true;
+    int unit_count = 0;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+      int bh, b, qt0;
+      unit_coords(u, bh, b, qt0);
+      const int kv_len = kv_len_of(mk, b);
+      const int n_kv = (kv_len + kTile - 1) / kTile;
+      int jmax = n_kv;
+      if (mk.causal && qt0 + 2 < jmax) jmax = qt0 + 2;
+      if (unit_count > 0 && !mbar_wait_warp(b_q_empty, (unit_count - 1) & 1, tmo, abort_flag)) {
+        fail();
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        for (int x = 0; x < 2; ++x) {
+          mbar_expect_tx(b_q_full[x], 2 * L::kTileBytes);
+          for (int c = 0; c < L::kChunks; ++c) {
+            tma_load_3d(sQ + x * L::kTileBytes + c * 16384, &tm_q, c * 64, (qt0 + x) * kTile, bh,
+                        b_q_full[x]);
+            tma_load_3d(sDO + x * L::kTileBytes + c * 16384, &tm_do, c * 64, (qt0 + x) * kTile,
+                        bh, b_q_full[x]);
+          }
+        }
+      }
+      ++q_arms;
+      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+        uint32_t bits = warp_valid_bits(mk, qt0, chunk, n_q, n_kv) |
+                        warp_valid_bits(mk, qt0 + 1, chunk, n_q, n_kv);
+        while (bits != 0u) {
+          const int j = chunk * 32 + (__ffs(bits) - 1);
+          bits &= bits - 1;
+          const int ks = it % L::kKStages, vs = it % L::kVStages;
+          const uint32_t kph = (it / L::kKStages) & 1u, vph = (it / L::kVStages) & 1u;
+          if (!mbar_wait_warp(b_k_empty[ks], kph ^ 1u, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_expect_tx(b_k_full[ks], L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_3d(sK + ks * L::kTileBytes + c * 16384, &tm_k, c * 64, j * kTile, bh,
+                          b_k_full[ks]);
+          }
+          ++k_arms;
+          if (!mbar_wait_warp(b_v_empty[vs], vph ^ 1u, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_expect_tx(b_v_full[vs], L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_3d(sV + vs * L::kTileBytes + c * 16384, &tm_v, c * 64, j * kTile, bh,
+                          b_v_full[vs]);
+          }
+          ++v_arms;
+          ++it;
+        }
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < L::kKStages; ++s)
+      if (k_arms > static_cast<uint32_t>(s))
+        mbar_wait_warp(b_k_full[s], ((k_arms - 1 - s) / L::kKStages) & 1, tmo, nullptr);
+#pragma unroll
+    for (int s = 0; s < L::kVStages; ++s)
+      if (v_arms > static_cast<uint32_t>(s))
+        mbar_wait_warp(b_v_full[s], ((v_arms - 1 - s) / L::kVStages) & 1, tmo, nullptr);
+    if (q_arms) {
+      mbar_wait_warp(b_q_full[0], (q_arms - 1) & 1, tmo, nullptr);
+      mbar_wait_warp(b_q_full[1], (q_arms - 1) & 1, tmo, nullptr);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t kIdDq = idesc_bf16_f32(128, D, 0, 1);
+    const bool elected = lane == 0;
+    uint32_t it = 0;
+    uint32_t sp_cnt[2] = {0, 0}, ds_cnt[2] = {0, 0};
+    bool ok = true;
+    int unit_count = 0;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+      int bh, b, qt0;
+      unit_coords(u, bh, b, qt0);
+      (void)bh;
+      const int kv_len = kv_len_of(mk, b);
+      const int n_kv = (kv_len + kTile - 1) / kTile;
+      int jmax = n_kv;
+      if (mk.causal && qt0 + 2 < jmax) jmax = qt0 + 2;
+      const uint32_t uph = unit_count & 1;
+      if (!mbar_wait_warp(b_q_full[0], uph, tmo, abort_flag) ||
+          !mbar_wait_warp(b_q_full[1], uph, tmo, abort_flag)) {
+        fail();
+        ok = false;
+        break;
+      }
+      bool pend[2] = {false, false};
+      bool first_dq[2] = {true, true};
+      int prev_ks = -1;
+      // dQ_x += dS_x K(prev): flush the tile of query tile x from the previous ring position.
+      auto flush_dq = [&](int x) -> bool {
+        if (!pend[x]) return true;
+        if (!mbar_wait_warp(b_ds_ready[x], ds_cnt[x] & 1, tmo, abort_flag)) return false;
+        ++ds_cnt[x];
+        if (first_dq[x] && unit_count > 0 &&
+            !mbar_wait_warp(b_dq_free[x], (unit_count - 1) & 1, tmo, abort_flag))
+          return false;
+        tc_fence_after();
+        if (elected) {
+          const uint64_t db = sdesc_sw128(sK + prev_ks * L::kTileBytes, 16384, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + L::col_dq(x), tmem + L::col_sp(x) + kk * 8,
+                   db + static_cast<uint64_t>((kk * 2048) >> 4), kIdDq,
+                   (first_dq[x] && kk == 0) ? 0u : 1u);
+        }
+        __syncwarp();
+        first_dq[x] = false;
+        pend[x] = false;
+        return true;
+      };
+      auto issue_ss = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+        const uint64_t da = sdesc_sw128(a_base, 16, 1024);
+        const uint64_t db = sdesc_sw128(b_base, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + d_col, da + (off >> 4), db + (off >> 4), kIdS, kk > 0 ? 1u : 0u);
+        }
+      };
+      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+        const uint32_t va = warp_valid_bits(mk, qt0, chunk, n_q, n_kv);
+        const uint32_t vb = warp_valid_bits(mk, qt0 + 1, chunk, n_q, n_kv);
+        uint32_t bits = va | vb;
+        while (bits != 0u) {
+          const int bit = __ffs(bits) - 1;
+          bits &= bits - 1;
+          const bool valid[2] = {((va >> bit) & 1u) != 0u, ((vb >> bit) & 1u) != 0u};
+          const int ks = it % L::kKStages, vs = it % L::kVStages;
+          const uint32_t kph = (it / L::kKStages) & 1u, vph = (it / L::kVStages) & 1u;
+          if (!mbar_wait_warp(b_k_full[ks], kph, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          if (prev_ks >= 0) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              if (ok && !flush_dq(x)) {
+                fail();
+                ok = false;
+              }
+            }
+            if (!ok) break;
+            if (elected) mma_commit(b_k_empty[prev_ks]);
+            __syncwarp();
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (valid[x]) {
+              if (elected) {
+                issue_ss(L::col_sp(x), sQ + x * L::kTileBytes, sK + ks * L::kTileBytes);
+                mma_commit(b_s_full[x]);
+              }
+              __syncwarp();
+            }
+          }
+          if (!mbar_wait_warp(b_v_full[vs], vph, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (!ok || !valid[x]) continue;
+            if (!mbar_wait_warp(b_sp_free[x], sp_cnt[x] & 1, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              continue;
+            }
+            ++sp_cnt[x];
+            tc_fence_after();
+            if (elected) {
+              issue_ss(L::col_sp(x), sDO + x * L::kTileBytes, sV + vs * L::kTileBytes);
+              mma_commit(b_dp_full[x]);
+            }
+            __syncwarp();
+            pend[x] = true;
+          }
+          if (!ok) break;
+          if (elected) mma_commit(b_v_empty[vs]);
+          __syncwarp();
+          prev_ks = ks;
+          ++it;
+        }
+      }
+      if (!ok) break;
+      if (prev_ks >= 0) {
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (ok && !flush_dq(x)) {
+            fail();
+            ok = false;
+          }
+        }
+        if (!ok) break;
+        if (elected) mma_commit(b_k_empty[prev_ks]);
+        __syncwarp();
+      }
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (ok && first_dq[x] && unit_count > 0 &&
+            !mbar_wait_warp(b_dq_free[x], (unit_count - 1) & 1, tmo, abort_flag)) {
+          fail();
+          ok = false;
+        }
+      }
+      if (!ok) break;
+      if (elected) {
+        mma_commit(b_dq_full[0]);
+        mma_commit(b_dq_full[1]);
+        mma_commit(b_q_empty);
+      }
+      __syncwarp();
+    }
+    if (elected) mma_commit(b_drain);
+    __syncwarp();
+    mbar_wait_warp(b_drain, 0, tmo, nullptr);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int x = warp >> 2;
+    const int quad = warp & 3;
+    const int t = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tSP = tmem + lane_base + L::col_sp(x);
+    const uint32_t tDQ = tmem + lane_base + L::col_dq(x);
+    const float c_log2 = args.scale_log2;
+    uint32_t s_cnt = 0, dp_cnt = 0;
+    bool ok = true;
+    int unit_count = 0;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+      int bh, b, qt0;
+      unit_coords(u, bh, b, qt0);
+      const int qt = qt0 + x;
+      const int row = qt * kTile + t;
+      const bool row_in = row < N;
+      const long long ridx = static_cast<long long>(bh) * N + row;
+      const float lse2 = lse2_of(args.lse, ridx, row_in);
+      const float dsum = row_in ? args.dsum[ridx] : 0.f;
+      const uint32_t row_global = static_cast<uint32_t>(ridx);
+      const int kv_len = kv_len_of(mk, b);
+      const int n_kv = (kv_len + kTile - 1) / kTile;
+      int jmax = n_kv;
+      if (mk.causal && qt + 1 < jmax) jmax = qt + 1;
+      int n_done = 0;
+      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+        uint32_t bits = warp_valid_bits(mk, qt, chunk, n_q, n_kv);
+        while (bits != 0u) {
+          const int j = chunk * 32 + (__ffs(bits) - 1);
+          bits &= bits - 1;
+          // dropout keep bits for keys [128 j, 128 j + 128) of this row
+          uint32_t zb[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+          if constexpr (DROPOUT) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const uint4 kw =
+                  dropout_keep16(args.drop, row_global, static_cast<uint32_t>(j * 8 + g));
+              const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+              uint32_t bits16 = 0;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) bits16 |= ((w4[e >> 2] >> (8 * (e & 3))) & 1u) << e;
+              zb[g >> 1] = (g & 1) ? ((zb[g >> 1] & 0xFFFFu) | (bits16 << 16)) : bits16;
+            }
+          }
+          const bool emask = tile_needs_element_mask(mk, qt, j, kv_len);
+          int lim = kv_len - j * kTile;
+          if (mk.causal) {
+            const int lc = row - j * kTile + 1;
+            lim = lc < lim ? lc : lim;
+          }
+          // ---- phase 1: P, kept packed in registers
+          if (!mbar_wait_warp(b_s_full[x], s_cnt & 1, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          ++s_cnt;
+          tc_fence_after();
+          uint32_t pp[64];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t sr[32];
+            tmem_ld32(tSP + 32 * c, sr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              float p0 = ex2_approx(fmaf(__uint_as_float(sr[k]), c_log2, -lse2));
+              float p1 = ex2_approx(fmaf(__uint_as_float(sr[k + 1]), c_log2, -lse2));
+              if (emask) {
+                p0 = (32 * c + k < lim) ? p0 : 0.f;
+                p1 = (32 * c + k + 1 < lim) ? p1 : 0.f;
+              }
+              pp[16 * c + k / 2] = pack_bf16x2(p0, p1);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(b_sp_free[x]);
+          // ---- phase 2: dS = P (Z dP / (1 - p) - D), written over dP as bf16
+          if (!mbar_wait_warp(b_dp_full[x], dp_cnt & 1, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          ++dp_cnt;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t dr[32];
+            tmem_ld32(tSP + 32 * c, dr);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const float2 pf =
+                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * c + k / 2]));
+              float z0 = args.drop.keep_scale, z1 = args.drop.keep_scale;
+              if constexpr (DROPOUT) {
+                z0 = ((zb[c] >> k) & 1u) ? z0 : 0.f;
+                z1 = ((zb[c] >> (k + 1)) & 1u) ? z1 : 0.f;
+              }
+              const float ds0 = pf.x * fmaf(z0, __uint_as_float(dr[k]), -dsum);
+              const float ds1 = pf.y * fmaf(z1, __uint_as_float(dr[k + 1]), -dsum);
+              pk[k / 2] = pack_bf16x2(ds0, ds1);
+            }
+            tmem_st16(tSP + 16 * c, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(b_ds_ready[x]);
+          ++n_done;
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue: dQ = scale * acc
+      if (!mbar_wait_warp(b_dq_full[x], unit_count & 1, tmo, abort_flag)) {
+        fail();
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      __nv_bfloat16* dst = args.dq + static_cast<size_t>(ridx) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        if (n_done > 0) {
+          tmem_ld32(tDQ + 32 * c, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          pk[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * args.scale,
+                              __uint_as_float(v[2 * k + 1]) * args.scale);
+        if (row_in) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(b_dq_free[x]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, int num_sms, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.mask.B) * a.mask.H * a.mask.N;
+  const long long want = (rows * 8 + 255) / 256;
+  const int grid = static_cast<int>(want < num_sms * 8LL ? want : num_sms * 8LL);
+  if (grid <= 0) return cudaSuccess;
+  if (d == 64)
+    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(a.o, a.dout, a.dsum, rows);
+  else
+    bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(a.o, a.dout, a.dsum, rows);
+  return cudaGetLastError();
+}
+
+template <int D, bool DROP>
+static cudaError_t launch_dkdv_impl(const CUtensorMap& tq, const CUtensorMap& tk,
+                                    const CUtensorMap& tv, const CUtensorMap& tdo,
+                                    const BwdArgs& a, int grid, cudaStream_t stream) {
+  auto kern = fa_bwd_dkdv_kernel<D, DROP>;
+  cudaError_t e = set_smem(kern, DkdvLayout<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kBwdThreads, DkdvLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+template <int D, bool DROP>
+static cudaError_t launch_dq_impl(const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                                  int grid, cudaStream_t stream) {
+  auto kern = fa_bwd_dq_kernel<D, DROP>;
+  cudaError_t e = set_smem(kern, DqLayout<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kBwdThreads, DqLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, int d, bool dropout,
+                            int num_sms, cudaStream_t stream) {
+  const int n_t = (a.mask.N + kTile - 1) / kTile;
+  const long long units = static_cast<long long>(a.mask.B) * a.mask.H * n_t;
+  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+  if (grid <= 0) return cudaSuccess;
+  if (d == 64)
+    return dropout ? launch_dkdv_impl<64, true>(tq, tk, tv, tdo, a, grid, stream)
+                   : launch_dkdv_impl<64, false>(tq, tk, tv, tdo, a, grid, stream);
+  return dropout ? launch_dkdv_impl<128, true>(tq, tk, tv, tdo, a, grid, stream)
+                 : launch_dkdv_impl<128, false>(tq, tk, tv, tdo, a, grid, stream);
+}
+
+cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& a, int d, bool dropout,
+                          int num_sms, cudaStream_t stream) {
+  const int n_q = (a.mask.N + kTile - 1) / kTile;
+  const long long units = static_cast<long long>(a.mask.B) * a.mask.H * ((n_q + 1) / 2);
+  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+  if (grid <= 0) return cudaSuccess;
+  if (d == 64)
+    return dropout ? launch_dq_impl<64, true>(tq, tk, tv, tdo, a, grid, stream)
+                   : launch_dq_impl<64, false>(tq, tk, tv, tdo, a, grid, stream);
+  return dropout ? launch_dq_impl<128, true>(tq, tk, tv, tdo, a, grid, stream)
+                 : launch_dq_impl<128, false>(tq, tk, tv, tdo, a, grid, stream);
+}
+
+}  // namespace fa

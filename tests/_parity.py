@@ -38,7 +38,8 @@ def lse_err(gpu, ref):
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     both_inf = np.isneginf(gpu) & np.isneginf(ref)
-    diff = np.where(both_inf, 0.0, np.abs(gpu - ref))
+    with np.errstate(invalid="ignore"):
+        diff = np.where(both_inf, 0.0, np.abs(gpu - ref))
     return float(np.max(diff)) if diff.size else 0.0
 
 
