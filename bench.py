@@ -1,0 +1,495 @@
+"""Benchmark: attention forward + backward TFLOP/s on one GB300 (or N replicas).
+
+One step = one forward (fa_fwd) and one backward (fa_bwd_preprocess,
+fa_bwd_dkdv, fa_bwd_dq) over one batch of the workload, inputs resident in
+device memory. FLOPs are algorithmic and counted over allowed (query, key)
+pairs P: forward 4 d P (two contractions), backward 10 d P (five), so a step
+is 14 d P. Kernels that recompute work (the dQ kernel recomputes S and dP)
+get no credit for it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                       [--impl ours|reference]
+Under torchrun every rank runs the same workload on its own GPU (the path
+shards by heads and batches; there is no data-path collective) and rank 0
+prints one JSON line with the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from io_aware_exact_07_gb300 import inputs  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "gpt2_medium"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
+# algorithmic flops per allowed pair for each tensor-core kernel (per unit of d)
+KERNEL_FLOPS_PER_PAIR_D = {"fwd": 4, "bwd_dkdv": 8, "bwd_dq": 6}
+
+
+# --------------------------------------------------------------------- work model
+
+def allowed_pairs(w: inputs.Workload, seqlens) -> int:
+    """Exact number of allowed (query, key) pairs over all heads."""
+    N, T = w.N, 128
+    nb = math.ceil(N / T)
+    mask = None
+    if w.butterfly:
+        i = np.arange(nb)[:, None]
+        j = np.arange(nb)[None, :]
+        x = i ^ j
+        mask = (x == 0) | ((x & (x - 1)) == 0)
+    lens = [N] * w.B if seqlens is None else [min(max(int(s), 0), N) for s in seqlens]
+    rows = np.arange(N)
+    total = 0
+    for L in lens:
+        if not w.causal and mask is None:
+            total += N * L
+            continue
+        if mask is None:  # causal, possibly padded: keys j <= i and j < L
+            total += int(np.minimum(rows + 1, L).sum())
+            continue
+        cnt = 0
+        for qt in range(nb):
+            r = rows[qt * T:(qt + 1) * T]
+            for kt in range(nb):
+                if not mask[qt, kt]:
+                    continue
+                lo, hi = kt * T, min((kt + 1) * T, L)
+                if hi <= lo:
+                    continue
+                hi_r = np.minimum(hi, r + 1) if w.causal else np.full_like(r, hi)
+                cnt += int(np.clip(hi_r - lo, 0, None).sum())
+        total += cnt
+    return total * w.H
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(os.path.join(ROOT, "io_aware_exact_07_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "io_aware_exact_07_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[workload][kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------------- our arm
+
+class Step:
+    """Device buffers and the four library calls of one fwd+bwd step."""
+
+    def __init__(self, w, x, dev):
+        import io_aware_exact_07_gb300 as fa
+        self.fa = fa
+        self.w = w
+        self.q, self.k, self.v, self.do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+        self.sl = None if x["seqlens"] is None else x["seqlens"].to(dev)
+        self.bm = None
+        if w.butterfly:
+            self.bm = fa.fa_butterfly_mask(math.ceil(w.N / 128)).to(dev)
+        B, H, N, d = w.B, w.H, w.N, w.d
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.opts = dict(causal=w.causal, dropout_p=w.dropout_p, seed=0, offset=0,
+                         block_mask=self.bm, seqlens_k=self.sl)
+
+    def run(self, events=None):
+        fa, w = self.fa, self.w
+        B, H, N, d, s = w.B, w.H, w.N, w.d, w.scale
+        o = self.opts
+        ev = events or [None] * 5
+        if ev[0] is not None:
+            ev[0].record()
+        st = fa.fa_fwd(self.q, self.k, self.v, self.o, self.lse, B, H, N, d, s, **o)
+        if ev[1] is not None:
+            ev[1].record()
+        st |= fa.fa_bwd_preprocess(self.o, self.do, B, H, N, d, self.ws, self.ws_bytes)
+        if ev[2] is not None:
+            ev[2].record()
+        st |= fa.fa_bwd_dkdv(self.q, self.k, self.v, self.do, self.lse, self.dk, self.dv, B, H,
+                             N, d, s, workspace=self.ws, workspace_bytes=self.ws_bytes, **o)
+        if ev[3] is not None:
+            ev[3].record()
+        st |= fa.fa_bwd_dq(self.q, self.k, self.v, self.do, self.lse, self.dq, B, H, N, d, s,
+                           workspace=self.ws, workspace_bytes=self.ws_bytes, **o)
+        if ev[4] is not None:
+            ev[4].record()
+        if st != 0:
+            raise RuntimeError(f"library call failed with status {st}")
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value: float) -> float:
+    if pg is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(w, x, seqlens, budget_s=15.0):
+    """Time the fp64 oracle (fwd + bwd) on a bounded sample of heads."""
+    import oracle
+    heads_all = [(b, h) for b in range(w.B) for h in range(w.H)]
+    sl_np = None if seqlens is None else seqlens.numpy()
+    bm = None
+    if w.butterfly:
+        bm = oracle.butterfly(math.ceil(w.N / 128))
+
+    def run(heads):
+        f64 = lambda t: np.stack([t[b, h].double().numpy() for b, h in heads])
+        q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
+        t0 = time.perf_counter()
+        kw = dict(causal=w.causal, dropout_p=w.dropout_p, seed=0, offset=0, block_mask=bm,
+                  seqlens_k=sl_np, heads=heads, H=w.H)
+        oracle.fwd(q, k, v, w.scale, **kw)
+        oracle.bwd(q, k, v, do, w.scale, **kw)
+        return time.perf_counter() - t0
+
+    t1 = run(heads_all[:1])
+    n = int(max(1, min(len(heads_all), budget_s / max(t1, 1e-6))))
+    sample = heads_all[:n]
+    t = run(sample) if n > 1 else t1
+    # allowed pairs of the sampled heads
+    per_b = {}
+    for b, h in sample:
+        per_b[b] = per_b.get(b, 0) + 1
+    pairs = 0
+    for b, cnt in per_b.items():
+        wb = inputs.Workload("s", 1, cnt, w.N, w.d, causal=w.causal, butterfly=w.butterfly)
+        pairs += allowed_pairs(wb, None if seqlens is None else [int(seqlens[b])])
+    flops = 14.0 * w.d * pairs
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.B * w.H} heads of {w.name}, fwd+bwd in fp64, {t:.1f} s",
+            "seconds": t}
+
+
+def measure_e2e(step, x, pg, stream, n_steps):
+    """Same step through the public calls with host buffers: each step copies its
+    inputs from pinned host memory and reads all results back."""
+    host_in = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+    host_out = {n: torch.empty(getattr(step, n).shape, dtype=getattr(step, n).dtype,
+                               pin_memory=True) for n in ("o", "lse", "dq", "dk", "dv")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        for n, t in host_in.items():
+            getattr(step, n).copy_(t, non_blocking=True)
+        step.run()
+        for n, t in host_out.items():
+            t.copy_(getattr(step, n), non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(pg)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return {"seconds": max_over_ranks(pg, e0.elapsed_time(e1) / 1e3), "h2d": h2d, "d2h": d2h,
+            "steps": n_steps}
+
+
+def run_ours(args, w):
+    world, rank, local, pg = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = inputs.draw(w, with_grad=True)
+    seqlens = x["seqlens"]
+    step = Step(w, x, dev)
+    pairs = allowed_pairs(w, None if seqlens is None else seqlens.tolist())
+    flops_step = 14.0 * w.d * pairs
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    # status word: a device-side timeout would be reported here
+    assert step.fa.fa_device_status() == 0, "device-side error during warm-up"
+
+    # ---- device-resident timed region, per-kernel events
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step.run(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(pg)
+    elapsed = start.elapsed_time(end) / 1e3
+    elapsed = max_over_ranks(pg, elapsed)
+    per_kernel = {k: [] for k in KERNELS}
+    for e in evs:
+        for j, k in enumerate(KERNELS):
+            per_kernel[k].append(e[j].elapsed_time(e[j + 1]) / 1e3)
+    kstats = {k: statistics.mean(v) for k, v in per_kernel.items()}
+    assert step.fa.fa_device_status() == 0, "device-side error during the timed region"
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(step, x, pg, stream, max(3, min(args.steps, 20)))
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return None
+
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    total_k = sum(kstats.values())
+    dominant = max(kstats, key=lambda k: kstats[k])
+    if dominant in KERNEL_FLOPS_PER_PAIR_D:
+        ach = KERNEL_FLOPS_PER_PAIR_D[dominant] * w.d * pairs / kstats[dominant] / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": ach / peak_sus}
+    else:
+        rows = w.B * w.H * w.N
+        byts = 2 * rows * w.d * 2 + rows * 4
+        ach = byts / kstats[dominant] / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
+    roof["kernel"] = dominant
+    roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
+    roof["traffic"] = ncu_traffic(dominant, w.name)
+    value = flops_step * args.steps * world / elapsed / 1e12
+    fwd_t, bwd_t = kstats["fwd"], total_k - kstats["fwd"]
+    fwd_tf = 4 * w.d * pairs / fwd_t / 1e12
+    bwd_tf = 10 * w.d * pairs / bwd_t / 1e12
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; no dataset)",
+        "config": {"workload": w.name, "description": w.description, "B": w.B, "H": w.H,
+                   "N": w.N, "d": w.d, "causal": w.causal, "dropout_p": w.dropout_p,
+                   "key_padding": w.padding, "block_mask": "butterfly" if w.butterfly else None,
+                   "allowed_pairs": pairs, "flops_per_step": flops_step,
+                   "l2": "inputs larger than L2 (no flush)" if 4 * w.B * w.H * w.N * w.d * 2 > 129e6
+                   else "inputs smaller than L2",
+                   "parallelism": f"replicas x{world} (heads are independent; no collective)"},
+        "pct_of_peak": {"burst": 100 * value / world / peak_burst,
+                        "sustained": 100 * value / world / peak_sus},
+        "breakdown": {"fwd_ms": fwd_t * 1e3, "bwd_ms": bwd_t * 1e3, "fwd_tflops": fwd_tf,
+                      "bwd_tflops": bwd_tf,
+                      "fwd_pct_burst_peak": 100 * fwd_tf / peak_burst,
+                      "bwd_pct_burst_peak": 100 * bwd_tf / peak_burst,
+                      "kernels_ms": {k: v * 1e3 for k, v in kstats.items()},
+                      "kernel_share": {k: v / total_k for k, v in kstats.items()}},
+        "roofline": roof,
+        "e2e": None if e2e is None else {
+            "value": flops_step * e2e["steps"] * world / e2e["seconds"] / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+            "steps": e2e["steps"]},
+        "gpu_launches": len(KERNELS) * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, x, seqlens)
+        result["cpu_baseline"].pop("seconds", None)
+    if pg is not None:
+        pg.destroy_process_group()
+    return result
+
+
+# -------------------------------------------------------------- reference arm
+
+def run_reference(args, w):
+    """The fp64 CPU oracle timed on the host cores, one bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    x = inputs.draw(w, with_grad=True)
+    seqlens = x["seqlens"]
+    sl_np = None if seqlens is None else seqlens.numpy()
+    bm = oracle.butterfly(math.ceil(w.N / 128)) if w.butterfly else None
+    heads = [(0, 0)]
+    f64 = lambda t: np.stack([t[b, h].double().numpy() for b, h in heads])
+    q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
+    kw = dict(causal=w.causal, dropout_p=w.dropout_p, seed=0, offset=0, block_mask=bm,
+              seqlens_k=sl_np, heads=heads, H=w.H)
+    wb = inputs.Workload("s", 1, 1, w.N, w.d, causal=w.causal, butterfly=w.butterfly)
+    pairs = allowed_pairs(wb, None if seqlens is None else [int(seqlens[0])])
+    flops = 14.0 * w.d * pairs
+
+    def one():
+        oracle.fwd(q, k, v, w.scale, **kw)
+        oracle.bwd(q, k, v, do, w.scale, **kw)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    t = time.perf_counter() - t0
+    value = flops * args.steps / t / 1e12
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    sample = f"head (0, 0) of {w.name} per step, fwd+bwd in fp64"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), same inputs)",
+        "config": {"workload": w.name, "description": w.description, "allowed_pairs": pairs,
+                   "flops_per_step": flops},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.ALL))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    w = inputs.ALL[args.workload]
+    if args.impl == "reference":
+        res = run_reference(args, w)
+    else:
+        res = run_ours(args, w)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
