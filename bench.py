@@ -228,6 +228,12 @@ def dist_setup(n_gpus):
     return world, rank, local, pg
 
 
+def whole_job_value(flops_step: float, steps: int, world: int, elapsed_max: float) -> float:
+    """TFLOP/s of the whole job: every rank ran `steps` steps of `flops_step`
+    (weak scaling), and the slowest rank's time bounds the job."""
+    return flops_step * steps * world / elapsed_max / 1e12
+
+
 def barrier(pg):
     if pg is not None:
         pg.barrier()
@@ -375,7 +381,7 @@ def run_ours(args, w):
     roof["kernel"] = dominant
     roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
     roof["traffic"] = ncu_traffic(dominant, w.name)
-    value = flops_step * args.steps * world / elapsed / 1e12
+    value = whole_job_value(flops_step, args.steps, world, elapsed)
     fwd_t, bwd_t = kstats["fwd"], total_k - kstats["fwd"]
     fwd_tf = 4 * w.d * pairs / fwd_t / 1e12
     bwd_tf = 10 * w.d * pairs / bwd_t / 1e12

@@ -1,0 +1,101 @@
+"""The C-ABI library loads and exports every symbol include/fa.h declares;
+host-side validation and host helpers work without a GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import io_aware_exact_07_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from io_aware_exact_07_gb300 import build
+    build.build()
+    return fa.load()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(fa.EXPORTS)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert fa.status_string(s)
+    assert fa.status_string(fa.FA_ERR_TIMEOUT) == "device-side wait timed out"
+
+
+def test_dropout_threshold_matches_oracle(lib):
+    for p in (0.0, 0.05, 0.1, 0.3, 0.5, 0.9, 255.4 / 256):
+        assert fa.fa_dropout_p8(p) == oracle.p8(p)
+    assert fa.fa_dropout_p8(-0.1) == -1
+    assert fa.fa_dropout_p8(1.0) == -1
+    assert fa.fa_dropout_p8(0.999) == -1  # rounds to 256: everything dropped, rejected
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 6, 8, 64, 128])
+def test_library_butterfly_equals_oracle_butterfly(lib, nb):
+    assert np.array_equal(fa.fa_butterfly_mask(nb).numpy(), oracle.butterfly(nb))
+
+
+def test_workspace_size(lib):
+    assert fa.fa_bwd_workspace_size(2, 3, 5, 64) == 256
+    assert fa.fa_bwd_workspace_size(64, 16, 1024, 64) == 64 * 16 * 1024 * 4
+    assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
+
+
+def _fwd_raw(lib, q=1 << 20, k=1 << 20, v=1 << 20, o=1 << 20, lse=1 << 20, B=1, H=1, N=128,
+             d=64, scale=0.125, p=0.0):
+    vp = ctypes.c_void_p
+    return lib.fa_fwd(vp(q), vp(k), vp(v), vp(o), vp(lse), B, H, N, d, scale, 0, p, 0, 0, None,
+                      None, None)
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    # every case is rejected on the host before any device work
+    assert _fwd_raw(lib, q=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_raw(lib, q=(1 << 20) + 8) == fa.FA_ERR_INVALID_ARG  # not 16-byte aligned
+    assert _fwd_raw(lib, lse=(1 << 20) + 2) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_raw(lib, N=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_raw(lib, B=-1) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_raw(lib, B=1 << 16, H=1 << 8, N=1 << 8) == fa.FA_ERR_INVALID_ARG  # B*H*N >= 2^31
+    assert _fwd_raw(lib, scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_raw(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_raw(lib, p=1.0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_raw(lib, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd_raw(lib, d=256) == fa.FA_ERR_UNSUPPORTED
+    vp = ctypes.c_void_p
+    a = vp(1 << 20)
+    # missing workspace for the backward
+    st = lib.fa_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 64, 0.125, 0, 0.0, 0, 0, None, None,
+                    None, 0, None)
+    assert st == fa.FA_ERR_WORKSPACE
+    st = lib.fa_bwd(a, a, a, a, a, a, a, a, a, 1, 1, 128, 64, 0.125, 0, 0.0, 0, 0, None, None, a,
+                    16, None)
+    assert st == fa.FA_ERR_WORKSPACE
+    assert lib.fa_debug_philox(vp(0), a, 4, 0, 0, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_product_path_has_no_fallback(monkeypatch, tmp_path):
+    """Without the built library the binding raises instead of computing elsewhere."""
+    import importlib
+    import io_aware_exact_07_gb300 as mod
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(RuntimeError):
+        mod.load()
