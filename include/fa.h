@@ -90,6 +90,49 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
                  size_t workspace_bytes, void* stream);
 
+/* The three stages fa_bwd runs, for callers that schedule or time them
+ * separately. They must run in this order on one stream with the same
+ * workspace (it carries D from the first stage to the other two); dK/dV and
+ * dQ are independent of each other once D exists.
+ *   fa_bwd_preprocess: D = rowsum(dO * O) into the workspace.
+ *   fa_bwd_dkdv:       dK, dV (one CTA owns each 128-row key tile).
+ *   fa_bwd_dq:         dQ (one CTA owns each 128-row query tile). */
+fa_status fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int N, int d,
+                            void* workspace, size_t workspace_bytes, void* stream);
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout,
+                      const float* lse, void* dk, void* dv, int B, int H, int N, int d,
+                      float scale, int causal, float dropout_p, uint64_t seed, uint64_t offset,
+                      const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                      size_t workspace_bytes, void* stream);
+fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
+                    const float* lse, void* dq, int B, int H, int N, int d, float scale,
+                    int causal, float dropout_p, uint64_t seed, uint64_t offset,
+                    const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* fa_bwd without a caller-provided workspace: for callers that cannot allocate
+ * device memory themselves, such as plugins inside a host framework that owns
+ * all device memory and offers them no workspace, or code that must not call
+ * cudaMalloc / cudaFree because those can synchronise the device or fail under
+ * a fixed memory budget. This entry point allocates nothing: D = rowsum(dO * O)
+ * goes to a static device array of 2^22 floats (16 MiB) that every GPU loading
+ * the library holds until the process exits. The pages have no counterpart of
+ * this call; it exists only for such callers.
+ *   - Arguments and outputs are exactly those of fa_bwd minus the workspace.
+ *   - B*H*N above 2^22 (4,194,304 query rows) is rejected with FA_ERR_WORKSPACE
+ *     before any device work.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - All calls on a device share the one array. Its contents left by an earlier
+ *     call do not matter (D is fully rewritten before it is read), but two calls
+ *     whose kernels overlap on the GPU (different streams, or one device used
+ *     from several threads without ordering) race on it: order them. */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, float dropout_p,
+                         uint64_t seed, uint64_t offset, const uint8_t* block_mask,
+                         const int32_t* seqlens_k, void* stream);
+
 /* Quantised dropout threshold round(256 p) used by fa_fwd / fa_bwd (-1 if p is
  * outside [0, 1)). The effective dropout rate is fa_dropout_p8(p) / 256. */
 int fa_dropout_p8(float dropout_p);

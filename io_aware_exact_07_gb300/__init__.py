@@ -31,7 +31,8 @@ FA_ERR_TIMEOUT = 5
 
 # Symbols declared in include/fa.h.
 EXPORTS = (
-    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_dropout_p8", "fa_debug_dropout_keep",
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq",
+    "fa_bwd_noalloc", "fa_dropout_p8", "fa_debug_dropout_keep",
     "fa_debug_philox", "fa_butterfly_mask", "fa_device_status", "fa_set_wait_timeout_ns",
     "fa_test_inject_stall", "fa_status_string",
 )
@@ -69,6 +70,17 @@ def load(build_if_missing: bool = False):
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u64,
                                vp, vp, vp, sz, vp]
         lib.fa_bwd.restype = i
+        lib.fa_bwd_preprocess.argtypes = [vp, vp, i, i, i, i, vp, sz, vp]
+        lib.fa_bwd_preprocess.restype = i
+        lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u64, vp,
+                                    vp, vp, sz, vp]
+        lib.fa_bwd_dkdv.restype = i
+        lib.fa_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u64, vp, vp,
+                                  vp, sz, vp]
+        lib.fa_bwd_dq.restype = i
+        lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f,
+                                       u64, u64, vp, vp, vp]
+        lib.fa_bwd_noalloc.restype = i
         lib.fa_dropout_p8.argtypes = [f]
         lib.fa_dropout_p8.restype = i
         lib.fa_debug_dropout_keep.argtypes = [vp, i, i, i, f, u64, u64, vp]
@@ -151,6 +163,43 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal=False, d
                          _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                          float(dropout_p), int(seed), int(offset), bm, sl, _ptr(workspace),
                          int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_preprocess(o, dout, B, H, N, d, workspace, workspace_bytes, stream=None) -> int:
+    return load().fa_bwd_preprocess(_ptr(o), _ptr(dout), B, H, N, d, _ptr(workspace),
+                                    int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_dkdv(q, k, v, dout, lse, dk, dv, B, H, N, d, scale, causal=False, dropout_p=0.0,
+                seed=0, offset=0, block_mask=None, seqlens_k=None, workspace=None,
+                workspace_bytes=0, stream=None) -> int:
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(dk),
+                              _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                              float(dropout_p), int(seed), int(offset), bm, sl, _ptr(workspace),
+                              int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_dq(q, k, v, dout, lse, dq, B, H, N, d, scale, causal=False, dropout_p=0.0, seed=0,
+              offset=0, block_mask=None, seqlens_k=None, workspace=None, workspace_bytes=0,
+              stream=None) -> int:
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(dq), B, H, N,
+                            d, float(scale), int(bool(causal)), float(dropout_p), int(seed),
+                            int(offset), bm, sl, _ptr(workspace), int(workspace_bytes),
+                            _stream(stream))
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal=False,
+                   dropout_p=0.0, seed=0, offset=0, block_mask=None, seqlens_k=None,
+                   stream=None) -> int:
+    """fa_bwd for callers that cannot allocate device memory: the library uses
+    its own static device scratch (B*H*N <= 2^22) instead of a workspace."""
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                 int(bool(causal)), float(dropout_p), int(seed), int(offset), bm,
+                                 sl, _stream(stream))
 
 
 def fa_dropout_p8(p: float) -> int:

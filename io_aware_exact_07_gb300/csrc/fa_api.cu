@@ -140,6 +140,16 @@ fa::SyncParams make_sync(const DeviceInfo* di, bool consume_stall) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Backward workspace for fa_bwd_noalloc: room for D = rowsum(dO * O) of up to
+// kNoAllocMaxRows query rows (B*H*N), 16 MiB. It is part of the library's
+// device image, so every GPU that loads the library holds it until the
+// process exits. In host code `g_noalloc_dsum` is only a host-side stand-in
+// for the array; its device address comes from cudaGetSymbolAddress below.
+constexpr size_t kNoAllocMaxRows = static_cast<size_t>(1) << 22;
+__device__ __align__(256) float g_noalloc_dsum[kNoAllocMaxRows];
+void* g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
 }  // namespace
 
 extern "C" {
@@ -177,46 +187,148 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return round256(static_cast<size_t>(B) * H * N * sizeof(float));
 }
 
+// Shared validation and set-up of the backward stages. `need` selects which
+// pointers must be present: 1 = preprocess (o, dout), 2 = dK/dV, 4 = dQ.
+static fa_status bwd_prepare(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             int B, int H, int N, int d, float scale, int causal, float dropout_p,
+                             uint64_t seed, uint64_t offset, const uint8_t* block_mask,
+                             const int32_t* seqlens_k, void* workspace, size_t workspace_bytes,
+                             int need, fa::BwdArgs* a, CUtensorMap* maps, DeviceInfo** di) {
+  fa_status st = check_common(B, H, N, d, scale, dropout_p);
+  if (st != FA_OK) return st;
+  if (need & 1) {
+    if (!o || !dout || !aligned16(o) || !aligned16(dout)) return FA_ERR_INVALID_ARG;
+  }
+  if (need & 6) {
+    if (!q || !k || !v || !dout || !lse) return FA_ERR_INVALID_ARG;
+    for (const void* p : {q, k, v, dout})
+      if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  }
+  if ((need & 2) && (!dk || !dv || !aligned16(dk) || !aligned16(dv))) return FA_ERR_INVALID_ARG;
+  if ((need & 4) && (!dq || !aligned16(dq))) return FA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < fa_bwd_workspace_size(B, H, N, d) ||
+      !aligned16(workspace))
+    return FA_ERR_WORKSPACE;
+  if ((st = device_info(di)) != FA_OK) return st;
+  if (need & 6) {
+    if (!encode_map(&maps[0], q, B * H, N, d) || !encode_map(&maps[1], k, B * H, N, d) ||
+        !encode_map(&maps[2], v, B * H, N, d) || !encode_map(&maps[3], dout, B * H, N, d))
+      return FA_ERR_CUDA;
+  }
+  a->mask = make_mask(B, H, N, causal, block_mask, seqlens_k);
+  a->drop = make_drop(dropout_p, seed, offset);
+  a->sync = make_sync(*di, false);
+  a->scale = scale;
+  a->scale_log2 = scale * fa::kLog2e;
+  a->o = static_cast<const __nv_bfloat16*>(o);
+  a->dout = static_cast<const __nv_bfloat16*>(dout);
+  a->lse = lse;
+  a->dsum = static_cast<float*>(workspace);
+  a->dq = static_cast<__nv_bfloat16*>(dq);
+  a->dk = static_cast<__nv_bfloat16*>(dk);
+  a->dv = static_cast<__nv_bfloat16*>(dv);
+  return FA_OK;
+}
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                  float scale, int causal, float dropout_p, uint64_t seed, uint64_t offset,
                  const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
                  size_t workspace_bytes, void* stream) {
-  fa_status st = check_common(B, H, N, d, scale, dropout_p);
-  if (st != FA_OK) return st;
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq),
-                        static_cast<const void*>(dk), static_cast<const void*>(dv)})
-    if (!aligned16(p)) return FA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
-  if (workspace == nullptr || workspace_bytes < fa_bwd_workspace_size(B, H, N, d) ||
-      !aligned16(workspace))
-    return FA_ERR_WORKSPACE;
-  DeviceInfo* di = nullptr;
-  if ((st = device_info(&di)) != FA_OK) return st;
-  CUtensorMap tq, tk, tv, tdo;
-  if (!encode_map(&tq, q, B * H, N, d) || !encode_map(&tk, k, B * H, N, d) ||
-      !encode_map(&tv, v, B * H, N, d) || !encode_map(&tdo, dout, B * H, N, d))
-    return FA_ERR_CUDA;
   fa::BwdArgs a;
-  a.mask = make_mask(B, H, N, causal, block_mask, seqlens_k);
-  a.drop = make_drop(dropout_p, seed, offset);
-  a.sync = make_sync(di, false);
-  a.scale = scale;
-  a.scale_log2 = scale * fa::kLog2e;
-  a.o = static_cast<const __nv_bfloat16*>(o);
-  a.dout = static_cast<const __nv_bfloat16*>(dout);
-  a.lse = lse;
-  a.dsum = static_cast<float*>(workspace);
-  a.dq = static_cast<__nv_bfloat16*>(dq);
-  a.dk = static_cast<__nv_bfloat16*>(dk);
-  a.dv = static_cast<__nv_bfloat16*>(dv);
+  CUtensorMap m[4];
+  DeviceInfo* di = nullptr;
+  fa_status st = bwd_prepare(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                             dropout_p, seed, offset, block_mask, seqlens_k, workspace,
+                             workspace_bytes, 7, &a, m, &di);
+  if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool drop = a.drop.p8 > 0;
   cudaError_t e = fa::launch_bwd_preprocess(a, d, di->num_sms, s);
-  if (e == cudaSuccess) e = fa::launch_bwd_dkdv(tq, tk, tv, tdo, a, d, drop, di->num_sms, s);
-  if (e == cudaSuccess) e = fa::launch_bwd_dq(tq, tk, tv, tdo, a, d, drop, di->num_sms, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_dkdv(m[0], m[1], m[2], m[3], a, d, drop, di->num_sms, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_dq(m[0], m[1], m[2], m[3], a, d, drop, di->num_sms, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int N, int d,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  fa::BwdArgs a;
+  CUtensorMap m[4];
+  DeviceInfo* di = nullptr;
+  fa_status st = bwd_prepare(nullptr, nullptr, nullptr, o, dout, nullptr, nullptr, nullptr,
+                             nullptr, B, H, N, d, 1.f, 0, 0.f, 0, 0, nullptr, nullptr, workspace,
+                             workspace_bytes, 1, &a, m, &di);
+  if (st != FA_OK) return st;
+  return fa::launch_bwd_preprocess(a, d, di->num_sms, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout,
+                      const float* lse, void* dk, void* dv, int B, int H, int N, int d,
+                      float scale, int causal, float dropout_p, uint64_t seed, uint64_t offset,
+                      const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  fa::BwdArgs a;
+  CUtensorMap m[4];
+  DeviceInfo* di = nullptr;
+  fa_status st = bwd_prepare(q, k, v, nullptr, dout, lse, nullptr, dk, dv, B, H, N, d, scale,
+                             causal, dropout_p, seed, offset, block_mask, seqlens_k, workspace,
+                             workspace_bytes, 2, &a, m, &di);
+  if (st != FA_OK) return st;
+  return fa::launch_bwd_dkdv(m[0], m[1], m[2], m[3], a, d, a.drop.p8 > 0, di->num_sms,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
+                    const float* lse, void* dq, int B, int H, int N, int d, float scale,
+                    int causal, float dropout_p, uint64_t seed, uint64_t offset,
+                    const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  fa::BwdArgs a;
+  CUtensorMap m[4];
+  DeviceInfo* di = nullptr;
+  fa_status st = bwd_prepare(q, k, v, nullptr, dout, lse, dq, nullptr, nullptr, B, H, N, d,
+                             scale, causal, dropout_p, seed, offset, block_mask, seqlens_k,
+                             workspace, workspace_bytes, 4, &a, m, &di);
+  if (st != FA_OK) return st;
+  return fa::launch_bwd_dq(m[0], m[1], m[2], m[3], a, d, a.drop.p8 > 0, di->num_sms,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, float dropout_p,
+                         uint64_t seed, uint64_t offset, const uint8_t* block_mask,
+                         const int32_t* seqlens_k, void* stream) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(N) > kNoAllocMaxRows)
+    return FA_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    // First call on this device (with it current): look up the array's device address.
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_dsum) != cudaSuccess || p == nullptr)
+        return FA_ERR_CUDA;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  // D is written in full by the first backward kernel before it is read, so
+  // the array's contents from an earlier call never matter and nothing is cleared.
+  return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dropout_p, seed,
+                offset, block_mask, seqlens_k, scratch, kNoAllocMaxRows * sizeof(float), stream);
 }
 
 int fa_dropout_p8(float dropout_p) { return p8_of(dropout_p); }
