@@ -50,19 +50,29 @@ struct FwdLayout {
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // barriers: q_full[2], q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
-  //           s_full[2], p_full[2], o_full[2], o_free[2], drain, stall
-  static constexpr int kNumBars = 2 + 1 + 4 * kStages + 8 + 2;
+  //           s_full[2], p_full[2], o_full[2], o_free[2], s_free[2], pv_done[2], drain, stall
+  static constexpr int kNumBars = 2 + 1 + 4 * kStages + 12 + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + slack for 1024-byte alignment
-  // tensor-memory columns
+  // At d = 64 tensor memory has room for a separate P buffer per query tile
+  // (2 x (128 S + 64 P + 64 O) = 512 columns), so the next S can be computed
+  // while the softmax still works on the current one. At d = 128 P is written
+  // over S (2 x (128 S + 128 O) = 512 columns).
+  static constexpr bool kSepP = (D == 64);
   __device__ static constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
-  __device__ static constexpr uint32_t col_o(int x) { return 256u + static_cast<uint32_t>(x * D); }
+  __device__ static constexpr uint32_t col_p(int x) {
+    return kSepP ? 256u + 64u * static_cast<uint32_t>(x) : col_s(x);
+  }
+  __device__ static constexpr uint32_t col_o(int x) {
+    return kSepP ? 384u + 64u * static_cast<uint32_t>(x) : 256u + static_cast<uint32_t>(x * D);
+  }
 };
 
 struct Bars {
   uint32_t q_full[2], q_empty;
   uint32_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint32_t s_full[2], p_full[2], o_full[2], o_free[2];
+  uint32_t s_free[2], pv_done[2];  // decoupled schedule only
   uint32_t drain, stall;
 };
 
@@ -126,6 +136,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int x = 0; x < 2; ++x) bars.p_full[x] = nb();
     for (int x = 0; x < 2; ++x) bars.o_full[x] = nb();
     for (int x = 0; x < 2; ++x) bars.o_free[x] = nb();
+    for (int x = 0; x < 2; ++x) bars.s_free[x] = nb();
+    for (int x = 0; x < 2; ++x) bars.pv_done[x] = nb();
     bars.drain = nb();
     bars.stall = nb();
   }
@@ -146,6 +158,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bars.p_full[x], 128);
       mbar_init(bars.o_full[x], 1);
       mbar_init(bars.o_free[x], 128);
+      mbar_init(bars.s_free[x], 128);
+      mbar_init(bars.pv_done[x], 1);
     }
     mbar_init(bars.drain, 1);
     mbar_init(bars.stall, 1);
@@ -255,20 +269,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // Lane 0 alone waits and issues: tcgen05.mma issue blocks while the tensor
+    // core is busy (its queue is shallow), so every cycle this thread spends on
+    // anything else is a tensor-core bubble. The rest of the warp only helps
+    // evaluate the tile lists (one ballot per 32 key tiles).
     constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
     constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);   // O += P V, V MN-major
+    constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
+    const bool leader = (lane == 0);
+    const uint64_t dQa = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dQb = sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
     uint32_t it = 0;
-    uint32_t p_cnt[2] = {0, 0};
+    uint32_t p_cnt0 = 0, p_cnt1 = 0, sf_cnt0 = 0, sf_cnt1 = 0;
+    bool s_seen0 = false, s_seen1 = false;
     bool ok = true;
-    bool issued_any = false;
-    const bool elected = (lane == 0);
-    if (args.sync.inject_stall) {
+    if (args.sync.inject_stall && leader) {
       // Test hook: this barrier is never completed, so the bounded wait runs out.
-      if (!mbar_wait_warp(bars.stall, 0, tmo, abort_flag)) {
+      if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
         fail();
         ok = false;
       }
     }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    auto issue_S = [&](int x, int s) {
+      const uint64_t dq = x ? dQb : dQa;
+      const uint64_t dk = dK0 + static_cast<uint64_t>(s) * kStageStep;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + L::col_s(x), dq + off, dk + off, kIdS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bars.s_full[x]);
+    };
+    auto issue_PV = [&](int x, int s, bool first) {
+      const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
+               dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
+               (first && kk == 0) ? 0u : 1u);
+    };
     int unit_count = 0;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
       const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
@@ -277,148 +319,137 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int jmax = n_kv;
       if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
       const uint32_t uph = unit_count & 1;
-      if (!mbar_wait_warp(bars.q_full[0], uph, tmo, abort_flag) ||
-          !mbar_wait_warp(bars.q_full[1], uph, tmo, abort_flag)) {
-        fail();
-        ok = false;
-        break;
-      }
-      bool pend[2] = {false, false};
-      bool first_pv[2] = {true, true};
+      bool pend0 = false, pend1 = false, first0 = true, first1 = true;
       int prev_stage = -1;
       uint32_t prev_ph = 0;
-
-      // PV for the tile of query tile x that was S-issued at the previous ring position.
-      auto flush_pv = [&](int x) -> bool {
-        if (!pend[x]) return true;
-        if (!mbar_wait_warp(bars.p_full[x], p_cnt[x] & 1, tmo, abort_flag)) return false;
-        ++p_cnt[x];
-        if (first_pv[x] && unit_count > 0) {
-          if (!mbar_wait_warp(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag)) return false;
-        }
+      // PV of query tile x for the tile S-issued at the previous ring position.
+      auto pv = [&](int x) -> bool {
+        uint32_t& pc = x ? p_cnt1 : p_cnt0;
+        bool& first = x ? first1 : first0;
+        if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
+        ++pc;
+        if (first && unit_count > 0 &&
+            !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
+          return false;
         tc_fence_after();
-        if (elected) {
-          const uint32_t vbase = sV + prev_stage * L::kTileBytes;
-          const uint64_t dv0 = sdesc_sw128(vbase, 16384, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            mma_ts(tmem + L::col_o(x), tmem + L::col_s(x) + kk * 8,
-                   dv0 + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
-                   (first_pv[x] && kk == 0) ? 0u : 1u);
-          }
-        }
-        __syncwarp();
-        first_pv[x] = false;
-        pend[x] = false;
+        issue_PV(x, prev_stage, first);
+        if constexpr (L::kSepP) mma_commit(bars.pv_done[x]);
+        first = false;
         return true;
       };
-
+      if (leader) {
+        ok = mbar_wait(bars.q_full[0], uph, tmo, abort_flag) &&
+             mbar_wait(bars.q_full[1], uph, tmo, abort_flag);
+        if (!ok) fail();
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
         const uint32_t va = warp_valid_bits(mk, uc.qt0, chunk, n_q, n_kv);
         const uint32_t vb = warp_valid_bits(mk, uc.qt0 + 1, chunk, n_q, n_kv);
-        uint32_t bits = va | vb;
-        while (bits != 0u) {
-          const int bit = __ffs(bits) - 1;
-          bits &= bits - 1;
-          const bool valid[2] = {((va >> bit) & 1u) != 0u, ((vb >> bit) & 1u) != 0u};
-          const int s = it % L::kStages;
-          const uint32_t ph = (it / L::kStages) & 1u;
-          if (!mbar_wait_warp(bars.k_full[s], ph, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          if (prev_stage >= 0) {
-            if (!mbar_wait_warp(bars.v_full[prev_stage], prev_ph, tmo, abort_flag)) {
-              fail();
+        if (leader) {
+          uint32_t bits = va | vb;
+          while (bits != 0u && ok) {
+            const int bit = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const bool v0 = ((va >> bit) & 1u) != 0u, v1 = ((vb >> bit) & 1u) != 0u;
+            const int s = it % L::kStages;
+            const uint32_t ph = (it / L::kStages) & 1u;
+            if (!mbar_wait(bars.k_full[s], ph, tmo, abort_flag)) {
               ok = false;
               break;
             }
-          }
-          tc_fence_after();
-          bool had_pv = pend[0] || pend[1];
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (!ok) break;
-            if (!flush_pv(x)) {
-              fail();
-              ok = false;
-              break;
-            }
-            if (valid[x]) {
-              if (elected) {
-                const uint32_t qb = sQ + x * L::kTileBytes;
-                const uint32_t kb = sK + s * L::kTileBytes;
-                const uint64_t dq0 = sdesc_sw128(qb, 16, 1024);
-                const uint64_t dk0 = sdesc_sw128(kb, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                  const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                  mma_ss(tmem + L::col_s(x), dq0 + (off >> 4), dk0 + (off >> 4), kIdS,
-                         kk > 0 ? 1u : 0u);
+            if constexpr (L::kSepP) {
+              // S of this position as soon as the softmax has read the previous S ...
+              if (v0) {
+                if (s_seen0 && !mbar_wait(bars.s_free[0], sf_cnt0++ & 1, tmo, abort_flag)) {
+                  ok = false;
+                  break;
                 }
-                mma_commit(bars.s_full[x]);
+                tc_fence_after();
+                issue_S(0, s);
+                s_seen0 = true;
               }
-              __syncwarp();
-              pend[x] = true;
-              issued_any = true;
+              if (v1) {
+                if (s_seen1 && !mbar_wait(bars.s_free[1], sf_cnt1++ & 1, tmo, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_S(1, s);
+                s_seen1 = true;
+              }
+              // ... then PV of the previous position, and release its V stage.
+              if (prev_stage >= 0) {
+                if (!mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag) ||
+                    (pend0 && !pv(0)) || (pend1 && !pv(1))) {
+                  ok = false;
+                  break;
+                }
+                mma_commit(bars.v_empty[prev_stage]);
+              }
+            } else {
+              // P is written over S: PV of the previous tile of x must be issued
+              // before the next S of x.
+              if (prev_stage >= 0 &&
+                  !mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const bool had_pv = pend0 || pend1;
+              if (pend0 && !pv(0)) {
+                ok = false;
+                break;
+              }
+              if (v0) issue_S(0, s);
+              if (pend1 && !pv(1)) {
+                ok = false;
+                break;
+              }
+              if (v1) issue_S(1, s);
+              if (had_pv) mma_commit(bars.v_empty[prev_stage]);
             }
-          }
-          if (!ok) break;
-          if (elected) {
-            if (had_pv) mma_commit(bars.v_empty[prev_stage]);
             mma_commit(bars.k_empty[s]);
+            pend0 = v0;
+            pend1 = v1;
+            prev_stage = s;
+            prev_ph = ph;
+            ++it;
           }
-          __syncwarp();
-          prev_stage = s;
-          prev_ph = ph;
-          ++it;
+          if (!ok) fail();
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      if (!ok) break;
-      // Flush the PVs of the last ring position, then release it.
-      if (prev_stage >= 0) {
-        if (!mbar_wait_warp(bars.v_full[prev_stage], prev_ph, tmo, abort_flag)) {
+      if (leader && ok) {
+        // Flush the PVs of the last position, then release it.
+        if (prev_stage >= 0) {
+          ok = mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag) &&
+               (!pend0 || pv(0)) && (!pend1 || pv(1));
+          if (ok) mma_commit(bars.v_empty[prev_stage]);
+        }
+        // A query tile without PV in this unit still consumes the epilogue
+        // handshake of the previous unit.
+        if (ok && first0 && unit_count > 0)
+          ok = mbar_wait(bars.o_free[0], (unit_count - 1) & 1, tmo, abort_flag);
+        if (ok && first1 && unit_count > 0)
+          ok = mbar_wait(bars.o_free[1], (unit_count - 1) & 1, tmo, abort_flag);
+        if (ok) {
+          if constexpr (!L::kSepP) {
+            mma_commit(bars.o_full[0]);
+            mma_commit(bars.o_full[1]);
+          }
+          mma_commit(bars.q_empty);
+        } else {
           fail();
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (ok && !flush_pv(x)) {
-            fail();
-            ok = false;
-          }
-        }
-        if (!ok) break;
-        if (elected) mma_commit(bars.v_empty[prev_stage]);
-        __syncwarp();
-      }
-      // A query tile with no PV in this unit still consumes the epilogue
-      // handshake of the previous unit.
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (ok && first_pv[x] && unit_count > 0) {
-          if (!mbar_wait_warp(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-          }
         }
       }
-      if (!ok) break;
-      if (elected) {
-        mma_commit(bars.o_full[0]);
-        mma_commit(bars.o_full[1]);
-        mma_commit(bars.q_empty);
-      }
-      __syncwarp();
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     // Drain: all issued MMAs must finish before tensor memory is released.
-    if (elected) mma_commit(bars.drain);
+    if (leader) {
+      mma_commit(bars.drain);
+      mbar_wait(bars.drain, 0, tmo, nullptr);
+    }
     __syncwarp();
-    mbar_wait_warp(bars.drain, 0, tmo, nullptr);
-    (void)issued_any;
   } else {
     // ------------------------------------------------------------ softmax
     const int x = warp >> 2;                 // query tile within the unit (0 = a, 1 = b)
@@ -426,9 +457,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int t = quad * 32 + lane;          // row within the query tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + L::col_s(x);
+    const uint32_t tP = tmem + lane_base + L::col_p(x);
     const uint32_t tO = tmem + lane_base + L::col_o(x);
     const float c_log2 = args.scale_log2;
     uint32_t s_cnt = 0;
+    uint32_t pv_cnt = 0;  // decoupled schedule: PV completions consumed
     bool ok = true;
     int unit_count = 0;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
@@ -460,6 +493,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, &sr[c * 32]);
           tmem_ld_wait();
+          if constexpr (L::kSepP) {
+            // S is in registers: the next S may be written over it.
+            tc_fence_before();
+            mbar_arrive(bars.s_free[x]);
+          }
           float s[128];
 #pragma unroll
           for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(sr[k]);
@@ -473,15 +511,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int k = 0; k < 128; ++k)
               if (k >= lim) s[k] = -INFINITY;
           }
-          float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+          float mx[16];
 #pragma unroll
-          for (int k = 4; k < 128; k += 4) {
-            mx0 = fmaxf(mx0, s[k]);
-            mx1 = fmaxf(mx1, s[k + 1]);
-            mx2 = fmaxf(mx2, s[k + 2]);
-            mx3 = fmaxf(mx3, s[k + 3]);
-          }
-          const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_log2;
+          for (int k = 0; k < 16; ++k) mx[k] = s[k];
+#pragma unroll
+          for (int k = 16; k < 128; ++k) mx[k & 15] = fmaxf(mx[k & 15], s[k]);
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
+          const float m_tile = mx[0] * c_log2;
           const float m_new = fmaxf(m_ref, m_tile);
           const bool grow = m_new > m_ref + kRescaleThreshold;
           float alpha = 1.f;
@@ -494,9 +533,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           // P = exp2(s*c - m_ref), summed (undropped) into l, dropout applied,
           // packed to bf16 and stored over S, 64 columns at a time.
           float rs0 = 0.f, rs1 = 0.f;
+          uint32_t pk[64];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            uint32_t pk[32];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               const int k0 = half * 64 + g * 16;
@@ -519,12 +558,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                   p0 = ((w[e >> 2] >> (8 * (e & 3))) & 0xFFu) ? p0 : 0.f;
                   p1 = ((w[(e + 1) >> 2] >> (8 * ((e + 1) & 3))) & 0xFFu) ? p1 : 0.f;
                 }
-                pk[g * 8 + (e >> 1)] = pack_bf16x2(p0, p1);
+                pk[half * 32 + g * 8 + (e >> 1)] = pack_bf16x2(p0, p1);
               }
             }
-            tmem_st32(tS + half * 32, pk);
+            if constexpr (!L::kSepP) tmem_st32(tS + half * 32, &pk[half * 32]);
           }
           l_sum += rs0 + rs1;
+          if constexpr (L::kSepP) {
+            // The previous PV reads the P buffer and accumulates into O: wait for it.
+            if (n_done > 0) {
+              if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
+                fail();
+                ok = false;
+                break;
+              }
+              ++pv_cnt;
+              tc_fence_after();
+            }
+          }
           // Rescale the O row in tensor memory (warp-collective loads/stores).
           if (n_done > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
@@ -537,6 +588,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               tmem_st32(tO + c * 32, o);
             }
           }
+          if constexpr (L::kSepP) {
+            tmem_st32(tP, &pk[0]);
+            tmem_st32(tP + 32, &pk[32]);
+          }
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bars.p_full[x]);
@@ -545,10 +600,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: O = acc * keep_scale / l, lse = (m + log2 l) * ln 2
-      if (!mbar_wait_warp(bars.o_full[x], unit_count & 1, tmo, abort_flag)) {
-        fail();
-        ok = false;
-        break;
+      if constexpr (L::kSepP) {
+        // the last PV of this unit has completed once its pv_done phase has
+        if (n_done > 0) {
+          if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          ++pv_cnt;
+        }
+      } else {
+        if (!mbar_wait_warp(bars.o_full[x], unit_count & 1, tmo, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
       }
       tc_fence_after();
       const bool row_ok = row < N;
