@@ -35,9 +35,10 @@ namespace fa {
 
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kPvWarp = 10;  // second MMA issuer (decoupled schedule)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when m grows by > 2^8
 
 template <int D>
@@ -51,7 +52,7 @@ struct FwdLayout {
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // barriers: q_full[2], q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
   //           s_full[2], p_full[2], o_full[2], o_free[2], s_free[2], pv_done[2], drain, stall
-  static constexpr int kNumBars = 2 + 1 + 4 * kStages + 12 + 2;
+  static constexpr int kNumBars = 2 + 1 + 4 * kStages + 12 + 3;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + slack for 1024-byte alignment
   // At d = 64 tensor memory has room for a separate P buffer per query tile
@@ -73,7 +74,7 @@ struct Bars {
   uint32_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint32_t s_full[2], p_full[2], o_full[2], o_free[2];
   uint32_t s_free[2], pv_done[2];  // decoupled schedule only
-  uint32_t drain, stall;
+  uint32_t drain, drain2, stall;
 };
 
 struct UnitCoord {
@@ -139,6 +140,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int x = 0; x < 2; ++x) bars.s_free[x] = nb();
     for (int x = 0; x < 2; ++x) bars.pv_done[x] = nb();
     bars.drain = nb();
+    bars.drain2 = nb();
     bars.stall = nb();
   }
 
@@ -162,6 +164,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bars.pv_done[x], 1);
     }
     mbar_init(bars.drain, 1);
+    mbar_init(bars.drain2, 1);
     mbar_init(bars.stall, 1);
     fence_mbar_init();
   }
@@ -378,15 +381,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 issue_S(1, s);
                 s_seen1 = true;
               }
-              // ... then PV of the previous position, and release its V stage.
-              if (prev_stage >= 0) {
-                if (!mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag) ||
-                    (pend0 && !pv(0)) || (pend1 && !pv(1))) {
-                  ok = false;
-                  break;
-                }
-                mma_commit(bars.v_empty[prev_stage]);
-              }
+              // (the PVs come from the PV-issuer warp)
             } else {
               // P is written over S: PV of the previous tile of x must be issued
               // before the next S of x.
@@ -419,7 +414,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      if (leader && ok) {
+      if (leader && ok && L::kSepP) {
+        mma_commit(bars.q_empty);
+      } else if (leader && ok) {
         // Flush the PVs of the last position, then release it.
         if (prev_stage >= 0) {
           ok = mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag) &&
@@ -450,6 +447,85 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_wait(bars.drain, 0, tmo, nullptr);
     }
     __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    // Decoupled schedule only: O_x += P_x V_j as soon as P_x of key tile j is
+    // ready, from a second issuing thread, so that the tensor core keeps
+    // receiving work while the S issuer waits on its own barriers. Its MMAs are
+    // tracked by its own commits (pv_done, v_empty).
+    if constexpr (L::kSepP) {
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
+      const bool leader = (lane == 0);
+      const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
+      uint32_t it = 0, p_cnt0 = 0, p_cnt1 = 0;
+      bool ok = true;
+      int unit_count = 0;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+        const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
+        const int kv_len = kv_len_of(mk, uc.b);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        int jmax = n_kv;
+        if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
+        bool first0 = true, first1 = true;
+        auto pv = [&](int x, int s) -> bool {
+          uint32_t& pc = x ? p_cnt1 : p_cnt0;
+          bool& first = x ? first1 : first0;
+          if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
+          ++pc;
+          if (first && unit_count > 0 &&
+              !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
+            return false;
+          tc_fence_after();
+          const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
+                   dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
+                   (first && kk == 0) ? 0u : 1u);
+          mma_commit(bars.pv_done[x]);
+          first = false;
+          return true;
+        };
+        for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+          const uint32_t va = warp_valid_bits(mk, uc.qt0, chunk, n_q, n_kv);
+          const uint32_t vb = warp_valid_bits(mk, uc.qt0 + 1, chunk, n_q, n_kv);
+          if (leader) {
+            uint32_t bits = va | vb;
+            while (bits != 0u && ok) {
+              const int bit = __ffs(bits) - 1;
+              bits &= bits - 1;
+              const int s = it % L::kStages;
+              const uint32_t ph = (it / L::kStages) & 1u;
+              if (!mbar_wait(bars.v_full[s], ph, tmo, abort_flag) ||
+                  (((va >> bit) & 1u) && !pv(0, s)) || (((vb >> bit) & 1u) && !pv(1, s))) {
+                ok = false;
+                break;
+              }
+              mma_commit(bars.v_empty[s]);
+              ++it;
+            }
+            if (!ok) fail();
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        if (leader && ok) {
+          // A query tile without PV in this unit still consumes the epilogue
+          // handshake of the previous unit.
+          if (first0 && unit_count > 0)
+            ok = mbar_wait(bars.o_free[0], (unit_count - 1) & 1, tmo, abort_flag);
+          if (ok && first1 && unit_count > 0)
+            ok = mbar_wait(bars.o_free[1], (unit_count - 1) & 1, tmo, abort_flag);
+          if (!ok) fail();
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      if (leader) {
+        mma_commit(bars.drain2);
+        mbar_wait(bars.drain2, 0, tmo, nullptr);
+      }
+      __syncwarp();
+    }
   } else {
     // ------------------------------------------------------------ softmax
     const int x = warp >> 2;                 // query tile within the unit (0 = a, 1 = b)
