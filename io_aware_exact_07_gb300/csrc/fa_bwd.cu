@@ -1136,7 +1136,7 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
   const long long units = static_cast<long long>(a.mask.B) * a.mask.H * n_t;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   if (grid <= 0) return cudaSuccess;
-  if (d == 64) return launch_bwd_dkdv64(tq, tk, tv, tdo, a, dropout, num_sms, stream);
+  if (d == 64) return launch_bwd_dkdv_split(tq, tk, tv, tdo, a, d, dropout, num_sms, stream);
   return dropout ? launch_dkdv_impl<128, true>(tq, tk, tv, tdo, a, grid, stream)
                  : launch_dkdv_impl<128, false>(tq, tk, tv, tdo, a, grid, stream);
 }
@@ -1148,7 +1148,7 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const long long units = static_cast<long long>(a.mask.B) * a.mask.H * ((n_q + 1) / 2);
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   if (grid <= 0) return cudaSuccess;
-  if (d == 64) return launch_bwd_dq64(tq, tk, tv, tdo, a, dropout, num_sms, stream);
+  return launch_bwd_dq_split(tq, tk, tv, tdo, a, d, dropout, num_sms, stream);
   return dropout ? launch_dq_impl<128, true>(tq, tk, tv, tdo, a, grid, stream)
                  : launch_dq_impl<128, false>(tq, tk, tv, tdo, a, grid, stream);
 }

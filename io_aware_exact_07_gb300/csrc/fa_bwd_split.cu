@@ -1,16 +1,20 @@
-// Backward kernels for head dimension 64 (the same mathematics as fa_bwd.cu;
-// FlashAttention deep-read report, sections 2.5 and 3.3).
-//
-// At d = 64 tensor memory has room for separate bf16 buffers for the operands
-// that the compute warps produce (P^T and dS^T in the key-tile kernel, dS in
-// the query-tile kernel), so the next S / dP can be computed as soon as the
-// compute warps have *read* the current one instead of after it was consumed.
-// Two issuing warps feed the tensor core: one for the shared-memory x
-// shared-memory products (S, dP), one for the products that read the compute
-// warps' output from tensor memory (dV, dK, dQ); each waits only on its own
-// dependencies and tracks its own MMAs with its own commits. Sixteen compute
-// warps (four warpgroups, 32 of the 128 columns each) hide the latency of the
-// element-wise work.
+// Backward kernels (the mathematics of fa_bwd.cu; FlashAttention deep-read
+// report, sections 2.5 and 3.3), built from three kinds of warps:
+//   - two issuing warps feed the tensor core: "A" issues the products whose
+//     operands are both in shared memory (S^T, dP^T in the key-tile kernel;
+//     S, dP in the query-tile kernel), "B" the products that read the compute
+//     warps' bf16 output from tensor memory (dV, dK; dQ). Each waits only on
+//     its own dependencies and tracks its own MMAs with its own commits, so the
+//     tensor core keeps receiving work while the other waits;
+//   - sixteen compute warps (four warpgroups, 32 of the 128 columns each) do
+//     the element-wise work, enough warps per scheduler to hide its latency;
+//   - one producer warp streams tiles with TMA.
+// Where tensor memory has room (the key-tile kernel at d = 64, the query-tile
+// kernel at both head sizes) the bf16 operands produced by the compute warps
+// get their own buffers, so the next S / dP is computed as soon as the current
+// one has been *read*. In the key-tile kernel at d = 128 (dV, dK, S^T, dP^T
+// fill all 512 columns) P^T and dS^T are written over S^T and dP^T, and the
+// next S^T / dP^T waits until dV / dK have consumed them.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -21,17 +25,18 @@ namespace fa {
 
 namespace {
 
-constexpr int kD = 64;
 constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kProdWarp = 16;
-constexpr int kIssueAWarp = 17;  // S^T / dP^T (dK,dV kernel) or S / dP (dQ kernel)
-constexpr int kIssueBWarp = 18;  // dV, dK (dK,dV kernel) or dQ (dQ kernel)
+constexpr int kIssueAWarp = 17;
+constexpr int kIssueBWarp = 18;
 constexpr int kThreads = 19 * 32;
-constexpr int kTileBytes = kTile * kD * 2;  // 16 KB
-constexpr uint64_t kTileDesc = static_cast<uint64_t>(kTileBytes >> 4);
-constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
-constexpr uint32_t kIdTS = idesc_bf16_f32(128, kD, 0, 1);   // B operand MN-major
+
+template <int D>
+struct TileT {
+  static constexpr int kBytes = kTile * D * 2;
+  static constexpr int kChunks = D / 64;  // 64-column (128-byte swizzle) chunks of 16 KB
+};
 
 __device__ __forceinline__ float lse2_at(const float* lse, long long idx, bool in_range) {
   if (!in_range) return INFINITY;
@@ -39,40 +44,60 @@ __device__ __forceinline__ float lse2_at(const float* lse, long long idx, bool i
   return (l == -INFINITY) ? INFINITY : l * kLog2e;
 }
 
-// S (M=128, N=128, K=64) from two K-major shared-memory tiles.
-__device__ __forceinline__ void mma_ss_tile(uint32_t d_tmem, uint64_t da, uint64_t db) {
+template <int D>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, int row, int bh,
+                                         uint32_t bar) {
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
-    const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
-    mma_ss(d_tmem, da + off, db + off, kIdSS, kk > 0 ? 1u : 0u);
+  for (int c = 0; c < TileT<D>::kChunks; ++c)
+    tma_load_3d(dst + c * 16384, map, c * 64, row, bh, bar);
+}
+
+// D_tmem (M=128, N=128) = A * B^T over K = D, both K-major shared-memory tiles.
+template <int D>
+__device__ __forceinline__ void mma_ss_tile(uint32_t d_tmem, uint64_t da, uint64_t db) {
+  constexpr uint32_t kId = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, da + off, db + off, kId, kk > 0 ? 1u : 0u);
   }
 }
-// acc (M=128, N=64) += A[tmem, bf16, 128 x 128] * B[smem, 128 x 64, MN-major].
-__device__ __forceinline__ void mma_ts_tile(uint32_t d_tmem, uint32_t a_tmem, uint64_t db,
-                                            bool accumulate) {
+
+// acc (M=128, N=D) += A[tmem, bf16, 128 x 128] * B[smem, 128 x D, MN-major].
+// The 16-column K step kk of A sits at a_base + (kk / 2) * a_pair + (kk % 2) * 8
+// (a_pair = 16: contiguous buffer; 32: pairs written over the fp32 columns
+// each warpgroup read).
+template <int D>
+__device__ __forceinline__ void mma_ts_tile(uint32_t d_tmem, uint32_t a_base, uint32_t a_pair,
+                                            uint64_t db, bool accumulate) {
+  constexpr uint32_t kId = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 2048) >> 4), kIdTS,
-           (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts(d_tmem, a_base + (kk >> 1) * a_pair + (kk & 1) * 8,
+           db + static_cast<uint64_t>((kk * 2048) >> 4), kId, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ======================================================================== dK, dV
-// Tensor memory: dV [0,64), dK [64,128), S^T [128,256), dP^T [256,384),
-// P^T bf16 [384,448), dS^T bf16 [448,512).
+template <int D>
 struct DkdvL {
-  static constexpr int kStages = 3;
-  static constexpr int kKVOff = 0;                                   // 2 x (K, V)
-  static constexpr int kQOff = 4 * kTileBytes;
-  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kLseOff = kDOOff + kStages * kTileBytes;      // kStages x 128 fp32
+  static constexpr int T = TileT<D>::kBytes;
+  static constexpr bool kSepBuf = (D == 64);       // separate P^T / dS^T buffers
+  static constexpr int kKVBufs = (D == 64) ? 2 : 1;
+  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kKVOff = 0;                                   // kKVBufs x (K, V)
+  static constexpr int kQOff = kKVBufs * 2 * T;
+  static constexpr int kDOOff = kQOff + kStages * T;
+  static constexpr int kLseOff = kDOOff + kStages * T;               // kStages x 128 fp32
   static constexpr int kDsumOff = kLseOff + kStages * 512;
   static constexpr int kDropOff = kDsumOff + kStages * 512;          // 16 warps x 1 KB
   static constexpr int kBarOff = kDropOff + kComputeWarps * 1024;
-  static constexpr int kNumBars = 4 + 2 * kStages + 12;
+  static constexpr int kNumBars = 4 + 2 * 3 + 12;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
-  static constexpr uint32_t kColDV = 0, kColDK = 64, kColSt = 128, kColDPt = 256, kColP = 384,
-                            kColDS = 448;
+  static constexpr uint32_t kColDV = 0, kColDK = D, kColSt = 2 * D, kColDPt = 2 * D + 128;
+  static constexpr uint32_t kColP = kSepBuf ? 384u : kColSt;
+  static constexpr uint32_t kColDS = kSepBuf ? 448u : kColDPt;
+  static constexpr uint32_t kPair = kSepBuf ? 16u : 32u;  // A-operand pair stride (columns)
 };
 
 struct DkdvBars {
@@ -81,13 +106,14 @@ struct DkdvBars {
   uint32_t acc_full, acc_free, drain_a, drain_b;
 };
 
-template <bool DROPOUT>
+template <int D, bool DROPOUT>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_bwd_dkdv64_kernel(const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
-  using L = DkdvL;
+    fa_bwd_dkdv_split_kernel(const __grid_constant__ CUtensorMap tm_q,
+                             const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v,
+                             const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
+  using L = DkdvL<D>;
+  constexpr int T = L::T;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -111,8 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
     for (int b = 0; b < 2; ++b) bars.kv_full[b] = nb();
     for (int b = 0; b < 2; ++b) bars.kv_empty[b] = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.q_full[s] = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.q_empty[s] = nb();
+    for (int s = 0; s < 3; ++s) bars.q_full[s] = nb();
+    for (int s = 0; s < 3; ++s) bars.q_empty[s] = nb();
     bars.st_full = nb();
     bars.st_free = nb();
     bars.dpt_full = nb();
@@ -132,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.kv_full[b], 1);
       mbar_init(bars.kv_empty[b], 1);
     }
-    for (int s = 0; s < L::kStages; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(bars.q_full[s], 32);
       mbar_init(bars.q_empty[s], 2 + kComputeWarps);  // both issuers + every compute warp
     }
@@ -176,17 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bh = u / n_t, kt = u % n_t;
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
-      const int kb = unit_count & 1;
-      const int kuse = unit_count >> 1;
+      const int kb = unit_count % L::kKVBufs;
+      const int kuse = unit_count / L::kKVBufs;
       if (kuse > 0 && !mbar_wait_warp(bars.kv_empty[kb], (kuse - 1) & 1, tmo, abort_flag)) {
         fail();
         ok = false;
         break;
       }
       if (lane == 0) {
-        mbar_expect_tx(bars.kv_full[kb], 2 * kTileBytes);
-        tma_load_3d(sKV + (2 * kb) * kTileBytes, &tm_k, 0, kt * kTile, bh, bars.kv_full[kb]);
-        tma_load_3d(sKV + (2 * kb + 1) * kTileBytes, &tm_v, 0, kt * kTile, bh, bars.kv_full[kb]);
+        mbar_expect_tx(bars.kv_full[kb], 2 * T);
+        tma_tile<D>(sKV + (2 * kb) * T, &tm_k, kt * kTile, bh, bars.kv_full[kb]);
+        tma_tile<D>(sKV + (2 * kb + 1) * T, &tm_v, kt * kTile, bh, bars.kv_full[kb]);
       }
       ++kv_arms[kb];
       for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
@@ -215,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
           reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
           if (lane == 0) {
-            mbar_expect_tx(bars.q_full[s], 2 * kTileBytes);
-            tma_load_3d(sQ + s * kTileBytes, &tm_q, 0, qt * kTile, bh, bars.q_full[s]);
-            tma_load_3d(sDO + s * kTileBytes, &tm_do, 0, qt * kTile, bh, bars.q_full[s]);
+            mbar_expect_tx(bars.q_full[s], 2 * T);
+            tma_tile<D>(sQ + s * T, &tm_q, qt * kTile, bh, bars.q_full[s]);
+            tma_tile<D>(sDO + s * T, &tm_do, qt * kTile, bh, bars.q_full[s]);
           } else {
             mbar_arrive(bars.q_full[s]);
           }
@@ -226,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < L::kKVBufs; ++b)
       if (kv_arms[b]) mbar_wait_warp(bars.kv_full[b], (kv_arms[b] - 1) & 1, tmo, nullptr);
 #pragma unroll
     for (int s = 0; s < L::kStages; ++s)
@@ -234,23 +260,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_warp(bars.q_full[s], ((q_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
   } else if (warp == kIssueAWarp) {
     // ------------------------------------------------------------ S^T, dP^T issuer
+    // Before overwriting S^T (dP^T) it waits until the compute warps have read it
+    // (separate buffers), or until dV (dK) has consumed the P^T (dS^T) written
+    // over it (aliased buffers).
     const bool leader = lane == 0;
-    uint32_t it = 0, gt = 0, stf = 0, dpf = 0;
+    const uint32_t bar_s_ok = L::kSepBuf ? bars.st_free : bars.p_done;
+    const uint32_t bar_dp_ok = L::kSepBuf ? bars.dpt_free : bars.ds_done;
+    uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
     bool ok = true;
     int unit_count = 0;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
       const int bh = u / n_t, kt = u % n_t;
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
-      const int kb = unit_count & 1;
+      const int kb = unit_count % L::kKVBufs;
       (void)bh;
-      if (leader && !mbar_wait(bars.kv_full[kb], (unit_count >> 1) & 1, tmo, abort_flag)) {
+      if (leader &&
+          !mbar_wait(bars.kv_full[kb], (unit_count / L::kKVBufs) & 1, tmo, abort_flag)) {
         fail();
         ok = false;
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      const uint64_t dK = sdesc_sw128(sKV + (2 * kb) * kTileBytes, 16, 1024);
-      const uint64_t dV = sdesc_sw128(sKV + (2 * kb + 1) * kTileBytes, 16, 1024);
+      const uint64_t dK = sdesc_sw128(sKV + (2 * kb) * T, 16, 1024);
+      const uint64_t dV = sdesc_sw128(sKV + (2 * kb + 1) * T, 16, 1024);
       for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
         const uint32_t vbits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
         if (leader) {
@@ -258,19 +290,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = it % L::kStages;
             const uint32_t ph = (it / L::kStages) & 1u;
             if (!mbar_wait(bars.q_full[s], ph, tmo, abort_flag) ||
-                (gt > 0 && !mbar_wait(bars.st_free, stf++ & 1, tmo, abort_flag))) {
+                (gt > 0 && !mbar_wait(bar_s_ok, sfc++ & 1, tmo, abort_flag))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            mma_ss_tile(tmem + L::kColSt, dK, sdesc_sw128(sQ + s * kTileBytes, 16, 1024));
+            mma_ss_tile<D>(tmem + L::kColSt, dK, sdesc_sw128(sQ + s * T, 16, 1024));
             mma_commit(bars.st_full);
-            if (gt > 0 && !mbar_wait(bars.dpt_free, dpf++ & 1, tmo, abort_flag)) {
+            if (gt > 0 && !mbar_wait(bar_dp_ok, dfc++ & 1, tmo, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            mma_ss_tile(tmem + L::kColDPt, dV, sdesc_sw128(sDO + s * kTileBytes, 16, 1024));
+            mma_ss_tile<D>(tmem + L::kColDPt, dV, sdesc_sw128(sDO + s * T, 16, 1024));
             mma_commit(bars.dpt_full);
             mma_commit(bars.q_empty[s]);
             ++gt;
@@ -311,16 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            mma_ts_tile(tmem + L::kColDV, tmem + L::kColP,
-                        sdesc_sw128(sDO + s * kTileBytes, 16384, 1024), !first);
+            mma_ts_tile<D>(tmem + L::kColDV, tmem + L::kColP, L::kPair,
+                           sdesc_sw128(sDO + s * T, 16384, 1024), !first);
             mma_commit(bars.p_done);
             if (!mbar_wait(bars.ds_ready, dsc++ & 1, tmo, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            mma_ts_tile(tmem + L::kColDK, tmem + L::kColDS,
-                        sdesc_sw128(sQ + s * kTileBytes, 16384, 1024), !first);
+            mma_ts_tile<D>(tmem + L::kColDK, tmem + L::kColDS, L::kPair,
+                           sdesc_sw128(sQ + s * T, 16384, 1024), !first);
             mma_commit(bars.ds_done);
             mma_commit(bars.q_empty[s]);
             first = false;
@@ -356,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tSt = tmem + lane_base + L::kColSt + 32 * wg;
     const uint32_t tDPt = tmem + lane_base + L::kColDPt + 32 * wg;
-    const uint32_t tP = tmem + lane_base + L::kColP + 16 * wg;
-    const uint32_t tDS = tmem + lane_base + L::kColDS + 16 * wg;
+    const uint32_t tP = tmem + lane_base + L::kColP + L::kPair * wg;
+    const uint32_t tDS = tmem + lane_base + L::kColDS + L::kPair * wg;
     const float c_log2 = args.scale_log2;
     uint32_t* drop_scratch = reinterpret_cast<uint32_t*>(smem + L::kDropOff + warp * 1024);
     uint32_t it = 0, gt = 0, stc = 0, dpc = 0, pdc = 0, dsc = 0;
@@ -409,13 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          float p[32];
+          float p[32];  // P^T, fp32, kept until dS^T is formed
           {
             uint32_t sr[32];
             tmem_ld32(tSt, sr);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(bars.st_free);
+            if constexpr (L::kSepBuf) {
+              tc_fence_before();
+              mbar_arrive(bars.st_free);
+            }
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
               const float4 l4 = reinterpret_cast<const float4*>(lse_t)[c4];
@@ -432,20 +466,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               p[c] = (key_ok && (!mk.causal || key <= q0 + c)) ? p[c] : 0.f;
           }
           {
-            uint32_t pk[16];
+            uint32_t pk[16];  // dropped copy for dV
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const float a0 = ((zb >> (2 * c)) & 1u) ? p[2 * c] : 0.f;
               const float a1 = ((zb >> (2 * c + 1)) & 1u) ? p[2 * c + 1] : 0.f;
               pk[c] = pack_bf16x2(a0, a1);
             }
-            if (gt > 0) {  // the previous dV has finished reading the P^T buffer
-              if (!mbar_wait_warp(bars.p_done, pdc++ & 1, tmo, abort_flag)) {
-                fail();
-                ok = false;
-                break;
+            if constexpr (L::kSepBuf) {
+              if (gt > 0) {  // the previous dV has finished reading the P^T buffer
+                if (!mbar_wait_warp(bars.p_done, pdc++ & 1, tmo, abort_flag)) {
+                  fail();
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
               }
-              tc_fence_after();
             }
             tmem_st16(tP, pk);
             tmem_st_wait();
@@ -463,8 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t dr[32];
             tmem_ld32(tDPt, dr);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(bars.dpt_free);
+            if constexpr (L::kSepBuf) {
+              tc_fence_before();
+              mbar_arrive(bars.dpt_free);
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
@@ -480,13 +518,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
               pk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
             }
-            if (gt > 0) {  // the previous dK has finished reading the dS^T buffer
-              if (!mbar_wait_warp(bars.ds_done, dsc++ & 1, tmo, abort_flag)) {
-                fail();
-                ok = false;
-                break;
+            if constexpr (L::kSepBuf) {
+              if (gt > 0) {  // the previous dK has finished reading the dS^T buffer
+                if (!mbar_wait_warp(bars.ds_done, dsc++ & 1, tmo, abort_flag)) {
+                  fail();
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
               }
-              tc_fence_after();
             }
             tmem_st16(tDS, pk);
             tmem_st_wait();
@@ -501,36 +541,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- epilogue: dV (warpgroups 0, 1) and dK (2, 3), 32 columns each
+      // ---- epilogue: dV (warpgroups 0, 1) and dK (2, 3), D/2 columns each
       if (!mbar_wait_warp(bars.acc_full, unit_count & 1, tmo, abort_flag)) {
         fail();
         ok = false;
         break;
       }
       tc_fence_after();
+      constexpr int kHalf = D / 2;
       const bool is_dv = wg < 2;
-      const uint32_t tAcc = tmem + lane_base + (is_dv ? L::kColDV : L::kColDK) + 32 * (wg & 1);
+      const uint32_t tAcc =
+          tmem + lane_base + (is_dv ? L::kColDV : L::kColDK) + kHalf * (wg & 1);
       const float mult = is_dv ? args.drop.keep_scale : args.scale;
       __nv_bfloat16* dst = (is_dv ? args.dv : args.dk) +
-                           (static_cast<size_t>(bh) * N + static_cast<size_t>(key)) * kD +
-                           32 * (wg & 1);
-      uint32_t v[32];
-      if (n_done > 0) {
-        tmem_ld32(tAcc, v);
-        tmem_ld_wait();
-      } else {
+                           (static_cast<size_t>(bh) * N + static_cast<size_t>(key)) * D +
+                           kHalf * (wg & 1);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = 0u;
-      }
-      uint32_t pk[16];
+      for (int c = 0; c < kHalf / 32; ++c) {
+        uint32_t v[32];
+        if (n_done > 0) {
+          tmem_ld32(tAcc + 32 * c, v);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        pk[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mult, __uint_as_float(v[2 * k + 1]) * mult);
-      if (key < N) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+          for (int k = 0; k < 32; ++k) v[k] = 0u;
+        }
+        uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        for (int k = 0; k < 16; ++k)
+          pk[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mult,
+                              __uint_as_float(v[2 * k + 1]) * mult);
+        if (key < N) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
       }
       tc_fence_before();
       mbar_arrive(bars.acc_free);
@@ -547,18 +593,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ======================================================================== dQ
 // One unit = one (b, h) head and one 128-row query tile; the loop runs over
 // the key tiles it attends to. Tensor memory: S [0,128), dP [128,256),
-// dQ [256,320), dS bf16 [320,384).
+// dQ [256, 256+d), dS bf16 [256+d, 320+d).
+template <int D>
 struct DqL {
-  static constexpr int kKStages = 4;
-  static constexpr int kVStages = 3;
-  static constexpr int kQOff = 0;                                  // 2 x (Q, dO)
-  static constexpr int kKOff = 4 * kTileBytes;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-  static constexpr int kNumBars = 4 + 2 * kKStages + 2 * kVStages + 10;
+  static constexpr int T = TileT<D>::kBytes;
+  static constexpr int kQDBufs = (D == 64) ? 2 : 1;
+  static constexpr int kKStages = (D == 64) ? 4 : 3;
+  static constexpr int kVStages = (D == 64) ? 3 : 2;
+  static constexpr int kQOff = 0;                                  // kQDBufs x (Q, dO)
+  static constexpr int kKOff = kQDBufs * 2 * T;
+  static constexpr int kVOff = kKOff + kKStages * T;
+  static constexpr int kBarOff = kVOff + kVStages * T;
+  static constexpr int kNumBars = 4 + 2 * 4 + 2 * 3 + 10;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 320;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
 };
 
 struct DqBars {
@@ -567,13 +616,14 @@ struct DqBars {
   uint32_t drain_a, drain_b;
 };
 
-template <bool DROPOUT>
+template <int D, bool DROPOUT>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_bwd_dq64_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
-  using L = DqL;
+    fa_bwd_dq_split_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
+  using L = DqL<D>;
+  constexpr int T = L::T;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -595,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
     for (int b = 0; b < 2; ++b) bars.qd_full[b] = nb();
     for (int b = 0; b < 2; ++b) bars.qd_empty[b] = nb();
-    for (int s = 0; s < L::kKStages; ++s) bars.k_full[s] = nb();
-    for (int s = 0; s < L::kKStages; ++s) bars.k_empty[s] = nb();
-    for (int s = 0; s < L::kVStages; ++s) bars.v_full[s] = nb();
-    for (int s = 0; s < L::kVStages; ++s) bars.v_empty[s] = nb();
+    for (int s = 0; s < 4; ++s) bars.k_full[s] = nb();
+    for (int s = 0; s < 4; ++s) bars.k_empty[s] = nb();
+    for (int s = 0; s < 3; ++s) bars.v_full[s] = nb();
+    for (int s = 0; s < 3; ++s) bars.v_empty[s] = nb();
     bars.s_full = nb();
     bars.s_free = nb();
     bars.dp_full = nb();
@@ -616,11 +666,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.qd_full[b], 1);
       mbar_init(bars.qd_empty[b], 1);
     }
-    for (int s = 0; s < L::kKStages; ++s) {
+    for (int s = 0; s < 4; ++s) {
       mbar_init(bars.k_full[s], 1);
       mbar_init(bars.k_empty[s], 1);
     }
-    for (int s = 0; s < L::kVStages; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(bars.v_full[s], 1);
       mbar_init(bars.v_empty[s], 1);
     }
@@ -675,16 +725,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int jmax = kv_limit(qt, n_kv);
-      const int qb = unit_count & 1, use = unit_count >> 1;
+      const int qb = unit_count % L::kQDBufs, use = unit_count / L::kQDBufs;
       if (use > 0 && !mbar_wait_warp(bars.qd_empty[qb], (use - 1) & 1, tmo, abort_flag)) {
         fail();
         ok = false;
         break;
       }
       if (lane == 0) {
-        mbar_expect_tx(bars.qd_full[qb], 2 * kTileBytes);
-        tma_load_3d(sQD + (2 * qb) * kTileBytes, &tm_q, 0, qt * kTile, bh, bars.qd_full[qb]);
-        tma_load_3d(sQD + (2 * qb + 1) * kTileBytes, &tm_do, 0, qt * kTile, bh, bars.qd_full[qb]);
+        mbar_expect_tx(bars.qd_full[qb], 2 * T);
+        tma_tile<D>(sQD + (2 * qb) * T, &tm_q, qt * kTile, bh, bars.qd_full[qb]);
+        tma_tile<D>(sQD + (2 * qb + 1) * T, &tm_do, qt * kTile, bh, bars.qd_full[qb]);
       }
       ++qd_arms[qb];
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
@@ -699,8 +749,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (lane == 0) {
-            mbar_expect_tx(bars.k_full[ks], kTileBytes);
-            tma_load_3d(sK + ks * kTileBytes, &tm_k, 0, j * kTile, bh, bars.k_full[ks]);
+            mbar_expect_tx(bars.k_full[ks], T);
+            tma_tile<D>(sK + ks * T, &tm_k, j * kTile, bh, bars.k_full[ks]);
           }
           ++k_arms;
           if (!mbar_wait_warp(bars.v_empty[vs], ((it / L::kVStages) & 1u) ^ 1u, tmo, abort_flag)) {
@@ -709,8 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (lane == 0) {
-            mbar_expect_tx(bars.v_full[vs], kTileBytes);
-            tma_load_3d(sV + vs * kTileBytes, &tm_v, 0, j * kTile, bh, bars.v_full[vs]);
+            mbar_expect_tx(bars.v_full[vs], T);
+            tma_tile<D>(sV + vs * T, &tm_v, j * kTile, bh, bars.v_full[vs]);
           }
           ++v_arms;
           ++it;
@@ -725,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < L::kVStages; ++s)
       if (v_arms > static_cast<uint32_t>(s))
         mbar_wait_warp(bars.v_full[s], ((v_arms - 1 - s) / L::kVStages) & 1, tmo, nullptr);
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < L::kQDBufs; ++b)
       if (qd_arms[b]) mbar_wait_warp(bars.qd_full[b], (qd_arms[b] - 1) & 1, tmo, nullptr);
   } else if (warp == kIssueAWarp) {
     // ------------------------------------------------------------ S, dP issuer
@@ -739,14 +789,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int jmax = kv_limit(qt, n_kv);
-      const int qb = unit_count & 1;
-      if (leader && !mbar_wait(bars.qd_full[qb], (unit_count >> 1) & 1, tmo, abort_flag)) {
+      const int qb = unit_count % L::kQDBufs;
+      if (leader &&
+          !mbar_wait(bars.qd_full[qb], (unit_count / L::kQDBufs) & 1, tmo, abort_flag)) {
         fail();
         ok = false;
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      const uint64_t dQ = sdesc_sw128(sQD + (2 * qb) * kTileBytes, 16, 1024);
-      const uint64_t dDO = sdesc_sw128(sQD + (2 * qb + 1) * kTileBytes, 16, 1024);
+      const uint64_t dQ = sdesc_sw128(sQD + (2 * qb) * T, 16, 1024);
+      const uint64_t dDO = sdesc_sw128(sQD + (2 * qb + 1) * T, 16, 1024);
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
         const uint32_t vbits = warp_valid_bits(mk, qt, chunk, n_q, n_kv);
         if (leader) {
@@ -758,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            mma_ss_tile(tmem + L::kColS, dQ, sdesc_sw128(sK + ks * kTileBytes, 16, 1024));
+            mma_ss_tile<D>(tmem + L::kColS, dQ, sdesc_sw128(sK + ks * T, 16, 1024));
             mma_commit(bars.s_full);
             if (!mbar_wait(bars.v_full[vs], (it / L::kVStages) & 1u, tmo, abort_flag) ||
                 (gt > 0 && !mbar_wait(bars.dp_free, dfc++ & 1, tmo, abort_flag))) {
@@ -766,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            mma_ss_tile(tmem + L::kColDP, dDO, sdesc_sw128(sV + vs * kTileBytes, 16, 1024));
+            mma_ss_tile<D>(tmem + L::kColDP, dDO, sdesc_sw128(sV + vs * T, 16, 1024));
             mma_commit(bars.dp_full);
             mma_commit(bars.v_empty[vs]);
             ++gt;
@@ -809,8 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            mma_ts_tile(tmem + L::kColDQ, tmem + L::kColDS,
-                        sdesc_sw128(sK + ks * kTileBytes, 16384, 1024), !first);
+            mma_ts_tile<D>(tmem + L::kColDQ, tmem + L::kColDS, 16,
+                           sdesc_sw128(sK + ks * T, 16384, 1024), !first);
             mma_commit(bars.ds_done);
             mma_commit(bars.k_empty[ks]);
             first = false;
@@ -847,7 +898,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + L::kColS + 32 * wg;
     const uint32_t tDP = tmem + lane_base + L::kColDP + 32 * wg;
     const uint32_t tDS = tmem + lane_base + L::kColDS + 16 * wg;
-    const uint32_t tDQ = tmem + lane_base + L::kColDQ + 16 * wg;
+    constexpr int kQCols = D / 4;  // dQ columns written by each warpgroup
+    const uint32_t tDQ = tmem + lane_base + L::kColDQ + kQCols * wg;
     const float c_log2 = args.scale_log2;
     uint32_t gt = 0, sc = 0, dc = 0, ddc = 0;
     bool ok = true;
@@ -878,7 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               static_cast<uint32_t>(j * 8 + 2 * wg + g));
               const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
 #pragma unroll
-              for (int e = 0; e < 16; ++e) zb |= ((w4[e >> 2] >> (8 * (e & 3))) & 1u) << (16 * g + e);
+              for (int e = 0; e < 16; ++e)
+                zb |= ((w4[e >> 2] >> (8 * (e & 3))) & 1u) << (16 * g + e);
             }
           }
           int lim = 128;  // keys [0, lim) of this tile are allowed for this row
@@ -890,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const int lim_local = lim - 32 * wg;
-          // ---- P = exp2(S c - lse2)
+          // ---- P = exp2(S c - lse2), kept as bf16 pairs
           if (!mbar_wait_warp(bars.s_full, sc++ & 1, tmo, abort_flag)) {
             fail();
             ok = false;
@@ -950,30 +1003,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- epilogue: dQ = scale * acc, 16 columns per warpgroup
+      // ---- epilogue: dQ = scale * acc, D/4 columns per warpgroup
       if (!mbar_wait_warp(bars.dq_full, unit_count & 1, tmo, abort_flag)) {
         fail();
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t v[16];
+      uint32_t v[kQCols];
       if (n_done > 0) {
-        tmem_ld16(tDQ, v);
+        if constexpr (kQCols == 32) tmem_ld32(tDQ, v);
+        else tmem_ld16(tDQ, v);
         tmem_ld_wait();
       } else {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = 0u;
+        for (int k = 0; k < kQCols; ++k) v[k] = 0u;
       }
-      uint32_t o[8];
+      uint32_t o[kQCols / 2];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 0; k < kQCols / 2; ++k)
         o[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * args.scale,
                            __uint_as_float(v[2 * k + 1]) * args.scale);
       if (row_in) {
-        uint4* d4 = reinterpret_cast<uint4*>(args.dq + static_cast<size_t>(ridx) * kD + 16 * wg);
-        d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        uint4* d4 = reinterpret_cast<uint4*>(args.dq + static_cast<size_t>(ridx) * D + kQCols * wg);
+#pragma unroll
+        for (int k = 0; k < kQCols / 8; ++k)
+          d4[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
       }
       tc_fence_before();
       mbar_arrive(bars.dq_free);
@@ -988,38 +1043,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename K>
-cudaError_t set_smem64(K kern, int bytes) {
+cudaError_t set_smem_split(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D>
+cudaError_t launch_dkdv_split_d(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                                bool dropout, int grid, cudaStream_t stream) {
+  auto kern = dropout ? fa_bwd_dkdv_split_kernel<D, true> : fa_bwd_dkdv_split_kernel<D, false>;
+  cudaError_t e = set_smem_split(kern, DkdvL<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, DkdvL<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dq_split_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const BwdArgs& a, bool dropout, int grid,
+                              cudaStream_t stream) {
+  auto kern = dropout ? fa_bwd_dq_split_kernel<D, true> : fa_bwd_dq_split_kernel<D, false>;
+  cudaError_t e = set_smem_split(kern, DqL<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, DqL<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_dkdv64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& tdo, const BwdArgs& a, bool dropout, int num_sms,
-                              cudaStream_t stream) {
+cudaError_t launch_bwd_dkdv_split(const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                                  int d, bool dropout, int num_sms, cudaStream_t stream) {
   const int n_t = (a.mask.N + kTile - 1) / kTile;
   const long long units = static_cast<long long>(a.mask.B) * a.mask.H * n_t;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   if (grid <= 0) return cudaSuccess;
-  auto kern = dropout ? fa_bwd_dkdv64_kernel<true> : fa_bwd_dkdv64_kernel<false>;
-  cudaError_t e = set_smem64(kern, DkdvL::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, DkdvL::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError();
+  return d == 64 ? launch_dkdv_split_d<64>(tq, tk, tv, tdo, a, dropout, grid, stream)
+                 : launch_dkdv_split_d<128>(tq, tk, tv, tdo, a, dropout, grid, stream);
 }
 
-cudaError_t launch_bwd_dq64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, bool dropout, int num_sms,
-                            cudaStream_t stream) {
+cudaError_t launch_bwd_dq_split(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                                int d, bool dropout, int num_sms, cudaStream_t stream) {
   const int n_q = (a.mask.N + kTile - 1) / kTile;
   const long long units = static_cast<long long>(a.mask.B) * a.mask.H * n_q;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   if (grid <= 0) return cudaSuccess;
-  auto kern = dropout ? fa_bwd_dq64_kernel<true> : fa_bwd_dq64_kernel<false>;
-  cudaError_t e = set_smem64(kern, DqL::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, DqL::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError();
+  return d == 64 ? launch_dq_split_d<64>(tq, tk, tv, tdo, a, dropout, grid, stream)
+                 : launch_dq_split_d<128>(tq, tk, tv, tdo, a, dropout, grid, stream);
 }
 
 }  // namespace fa

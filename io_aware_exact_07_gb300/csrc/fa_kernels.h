@@ -46,13 +46,13 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const CUtensorMap& tdo, const BwdArgs& a, int d, bool dropout,
                           int num_sms, cudaStream_t stream);
 
-// Head dimension 64: decoupled two-issuer variants (fa_bwd64.cu).
-cudaError_t launch_bwd_dkdv64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const CUtensorMap& tdo, const BwdArgs& a, bool dropout, int num_sms,
-                              cudaStream_t stream);
-cudaError_t launch_bwd_dq64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, bool dropout, int num_sms,
-                            cudaStream_t stream);
+// Two-issuer backward kernels (fa_bwd_split.cu), d = 64 or 128.
+cudaError_t launch_bwd_dkdv_split(const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                                  int d, bool dropout, int num_sms, cudaStream_t stream);
+cudaError_t launch_bwd_dq_split(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                                int d, bool dropout, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_debug_dropout(uint8_t* keep, int B, int H, int N, const DropParams& d,
                                  cudaStream_t stream);
