@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t it = 0, kv_arms = 0, q_arms = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const int bh = u / n_t, kt = u % n_t;
       const int b = bh / mk.H;
       const int kv_len = kv_len_of(mk, b);
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_ss(tmem + d_col, da + (off >> 4), db + (off >> 4), kIdS, kk > 0 ? 1u : 0u);
       }
     };
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const int bh = u / n_t, kt = u % n_t;
       const int b = bh / mk.H;
       const int kv_len = kv_len_of(mk, b);
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t it = 0, st_cnt = 0, dpt_cnt = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const int bh = u / n_t, kt = u % n_t;
       const int b = bh / mk.H;
       const int kv_len = kv_len_of(mk, b);
@@ -571,523 +571,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// ================================================================== dQ
-// One work unit = one (b, h) head and 256 query rows (query tiles a and b);
-// the loop runs over the key tiles either tile attends to.
-//   warp 8      TMA producer: Q_a, Q_b, dO_a, dO_b per unit; K_j and V_j through
-//               separate rings (K is still needed for dQ after V is done).
-//   warp 9      MMA issuer: S_x = Q_x K^T, dP_x = dO_x V^T (shared-memory
-//               operands) and dQ_x += dS_x K (A from tensor memory).
-//   warps 0-7   one warpgroup per query tile (thread = query row): P = exp2(S c -
-//               lse2) kept packed as bf16 in registers while dP overwrites S in
-//               tensor memory; then dS = P (Z dP/(1-p) - D) written over dP.
-// Tensor memory: S/dP/dS of tile x at [128 x, 128 x + 128); dQ_x at 256 + x d.
-template <int D>
-struct DqLayout {
-  static constexpr int kChunks = D / 64;
-  static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kKStages = (D == 64) ? 4 : 2;
-  static constexpr int kVStages = (D == 64) ? 2 : 1;
-  static constexpr int kQOff = 0;                       // Q_a, Q_b
-  static constexpr int kDOOff = 2 * kTileBytes;         // dO_a, dO_b
-  static constexpr int kKOff = 4 * kTileBytes;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-  static constexpr int kNumBars = 3 + 2 * kKStages + 2 * kVStages + 12 + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
-  __device__ static constexpr uint32_t col_sp(int x) { return static_cast<uint32_t>(x) * 128u; }
-  __device__ static constexpr uint32_t col_dq(int x) { return 256u + static_cast<uint32_t>(x * D); }
-};
-
-template <int D, bool DROPOUT>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
-  using L = DqLayout<D>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const MaskParams& mk = args.mask;
-  const int N = mk.N;
-  const int BH = mk.B * mk.H;
-  const int n_q = (N + kTile - 1) / kTile;
-  const int n_qblk = (n_q + 1) / 2;
-  const int n_units = BH * n_qblk;
-
-  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff + 8);
-
-  uint32_t b_q_full[2], b_q_empty, b_k_full[4], b_k_empty[4], b_v_full[2], b_v_empty[2];
-  uint32_t b_s_full[2], b_sp_free[2], b_dp_full[2], b_ds_ready[2], b_dq_full[2], b_dq_free[2];
-  uint32_t b_drain;
-  {
-    int i = 0;
-    auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
-    b_q_full[0] = nb();
-    b_q_full[1] = nb();
-    b_q_empty = nb();
-    for (int s = 0; s < L::kKStages; ++s) b_k_full[s] = nb();
-    for (int s = 0; s < L::kKStages; ++s) b_k_empty[s] = nb();
-    for (int s = 0; s < L::kVStages; ++s) b_v_full[s] = nb();
-    for (int s = 0; s < L::kVStages; ++s) b_v_empty[s] = nb();
-    for (int x = 0; x < 2; ++x) {
-      b_s_full[x] = nb();
-      b_sp_free[x] = nb();
-      b_dp_full[x] = nb();
-      b_ds_ready[x] = nb();
-      b_dq_full[x] = nb();
-      b_dq_free[x] = nb();
-    }
-    b_drain = nb();
-  }
-  if (tid == 0) {
-    *abort_flag = 0;
-    mbar_init(b_q_full[0], 1);
-    mbar_init(b_q_full[1], 1);
-    mbar_init(b_q_empty, 1);
-    for (int s = 0; s < L::kKStages; ++s) {
-      mbar_init(b_k_full[s], 1);
-      mbar_init(b_k_empty[s], 1);
-    }
-    for (int s = 0; s < L::kVStages; ++s) {
-      mbar_init(b_v_full[s], 1);
-      mbar_init(b_v_empty[s], 1);
-    }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(b_s_full[x], 1);
-      mbar_init(b_sp_free[x], 128);
-      mbar_init(b_dp_full[x], 1);
-      mbar_init(b_ds_ready[x], 128);
-      mbar_init(b_dq_full[x], 1);
-      mbar_init(b_dq_free[x], 128);
-    }
-    mbar_init(b_drain, 1);
-    fence_mbar_init();
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint64_t tmo = args.sync.timeout_ns;
-  auto fail = [&]() {
-    *abort_flag = 1;
-    record_error(args.sync.status, kStatusTimeout);
-  };
-  const uint32_t sQ = smem_u32(smem + L::kQOff);
-  const uint32_t sDO = smem_u32(smem + L::kDOOff);
-  const uint32_t sK = smem_u32(smem + L::kKOff);
-  const uint32_t sV = smem_u32(smem + L::kVOff);
-
-  auto unit_coords = [&](int u, int& bh, int& b, int& qt0) {
-    bh = u / n_qblk;
-    int qb = u % n_qblk;
-    if (mk.causal) qb = n_qblk - 1 - qb;
-    b = bh / mk.H;
-    qt0 = 2 * qb;
-  };
-
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    uint32_t it = 0, k_arms = 0, v_arms = 0, q_arms = 0;
-    bool ok = true;
-    int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
-      int bh, b, qt0;
-      unit_coords(u, bh, b, qt0);
-      const int kv_len = kv_len_of(mk, b);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      int jmax = n_kv;
-      if (mk.causal && qt0 + 2 < jmax) jmax = qt0 + 2;
-      if (unit_count > 0 && !mbar_wait_warp(b_q_empty, (unit_count - 1) & 1, tmo, abort_flag)) {
-        fail();
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        for (int x = 0; x < 2; ++x) {
-          mbar_expect_tx(b_q_full[x], 2 * L::kTileBytes);
-          for (int c = 0; c < L::kChunks; ++c) {
-            tma_load_3d(sQ + x * L::kTileBytes + c * 16384, &tm_q, c * 64, (qt0 + x) * kTile, bh,
-                        b_q_full[x]);
-            tma_load_3d(sDO + x * L::kTileBytes + c * 16384, &tm_do, c * 64, (qt0 + x) * kTile,
-                        bh, b_q_full[x]);
-          }
-        }
-      }
-      ++q_arms;
-      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits(mk, qt0, chunk, n_q, n_kv) |
-                        warp_valid_bits(mk, qt0 + 1, chunk, n_q, n_kv);
-        while (bits != 0u) {
-          const int j = chunk * 32 + (__ffs(bits) - 1);
-          bits &= bits - 1;
-          const int ks = it % L::kKStages, vs = it % L::kVStages;
-          const uint32_t kph = (it / L::kKStages) & 1u, vph = (it / L::kVStages) & 1u;
-          if (!mbar_wait_warp(b_k_empty[ks], kph ^ 1u, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            mbar_expect_tx(b_k_full[ks], L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(sK + ks * L::kTileBytes + c * 16384, &tm_k, c * 64, j * kTile, bh,
-                          b_k_full[ks]);
-          }
-          ++k_arms;
-          if (!mbar_wait_warp(b_v_empty[vs], vph ^ 1u, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            mbar_expect_tx(b_v_full[vs], L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(sV + vs * L::kTileBytes + c * 16384, &tm_v, c * 64, j * kTile, bh,
-                          b_v_full[vs]);
-          }
-          ++v_arms;
-          ++it;
-        }
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < L::kKStages; ++s)
-      if (k_arms > static_cast<uint32_t>(s))
-        mbar_wait_warp(b_k_full[s], ((k_arms - 1 - s) / L::kKStages) & 1, tmo, nullptr);
-#pragma unroll
-    for (int s = 0; s < L::kVStages; ++s)
-      if (v_arms > static_cast<uint32_t>(s))
-        mbar_wait_warp(b_v_full[s], ((v_arms - 1 - s) / L::kVStages) & 1, tmo, nullptr);
-    if (q_arms) {
-      mbar_wait_warp(b_q_full[0], (q_arms - 1) & 1, tmo, nullptr);
-      mbar_wait_warp(b_q_full[1], (q_arms - 1) & 1, tmo, nullptr);
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t kIdDq = idesc_bf16_f32(128, D, 0, 1);
-    const bool elected = lane == 0;
-    uint32_t it = 0;
-    uint32_t sp_cnt[2] = {0, 0}, ds_cnt[2] = {0, 0};
-    bool ok = true;
-    int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
-      int bh, b, qt0;
-      unit_coords(u, bh, b, qt0);
-      (void)bh;
-      const int kv_len = kv_len_of(mk, b);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      int jmax = n_kv;
-      if (mk.causal && qt0 + 2 < jmax) jmax = qt0 + 2;
-      const uint32_t uph = unit_count & 1;
-      if (!mbar_wait_warp(b_q_full[0], uph, tmo, abort_flag) ||
-          !mbar_wait_warp(b_q_full[1], uph, tmo, abort_flag)) {
-        fail();
-        ok = false;
-        break;
-      }
-      bool pend[2] = {false, false};
-      bool first_dq[2] = {true, true};
-      int prev_ks = -1;
-      // dQ_x += dS_x K(prev): flush the tile of query tile x from the previous ring position.
-      auto flush_dq = [&](int x) -> bool {
-        if (!pend[x]) return true;
-        if (!mbar_wait_warp(b_ds_ready[x], ds_cnt[x] & 1, tmo, abort_flag)) return false;
-        ++ds_cnt[x];
-        if (first_dq[x] && unit_count > 0 &&
-            !mbar_wait_warp(b_dq_free[x], (unit_count - 1) & 1, tmo, abort_flag))
-          return false;
-        tc_fence_after();
-        if (elected) {
-          const uint64_t db = sdesc_sw128(sK + prev_ks * L::kTileBytes, 16384, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + L::col_dq(x), tmem + L::col_sp(x) + kk * 8,
-                   db + static_cast<uint64_t>((kk * 2048) >> 4), kIdDq,
-                   (first_dq[x] && kk == 0) ? 0u : 1u);
-        }
-        __syncwarp();
-        first_dq[x] = false;
-        pend[x] = false;
-        return true;
-      };
-      auto issue_ss = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
-        const uint64_t da = sdesc_sw128(a_base, 16, 1024);
-        const uint64_t db = sdesc_sw128(b_base, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + d_col, da + (off >> 4), db + (off >> 4), kIdS, kk > 0 ? 1u : 0u);
-        }
-      };
-      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        const uint32_t va = warp_valid_bits(mk, qt0, chunk, n_q, n_kv);
-        const uint32_t vb = warp_valid_bits(mk, qt0 + 1, chunk, n_q, n_kv);
-        uint32_t bits = va | vb;
-        while (bits != 0u) {
-          const int bit = __ffs(bits) - 1;
-          bits &= bits - 1;
-          const bool valid[2] = {((va >> bit) & 1u) != 0u, ((vb >> bit) & 1u) != 0u};
-          const int ks = it % L::kKStages, vs = it % L::kVStages;
-          const uint32_t kph = (it / L::kKStages) & 1u, vph = (it / L::kVStages) & 1u;
-          if (!mbar_wait_warp(b_k_full[ks], kph, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          if (prev_ks >= 0) {
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              if (ok && !flush_dq(x)) {
-                fail();
-                ok = false;
-              }
-            }
-            if (!ok) break;
-            if (elected) mma_commit(b_k_empty[prev_ks]);
-            __syncwarp();
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (valid[x]) {
-              if (elected) {
-                issue_ss(L::col_sp(x), sQ + x * L::kTileBytes, sK + ks * L::kTileBytes);
-                mma_commit(b_s_full[x]);
-              }
-              __syncwarp();
-            }
-          }
-          if (!mbar_wait_warp(b_v_full[vs], vph, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (!ok || !valid[x]) continue;
-            if (!mbar_wait_warp(b_sp_free[x], sp_cnt[x] & 1, tmo, abort_flag)) {
-              fail();
-              ok = false;
-              continue;
-            }
-            ++sp_cnt[x];
-            tc_fence_after();
-            if (elected) {
-              issue_ss(L::col_sp(x), sDO + x * L::kTileBytes, sV + vs * L::kTileBytes);
-              mma_commit(b_dp_full[x]);
-            }
-            __syncwarp();
-            pend[x] = true;
-          }
-          if (!ok) break;
-          if (elected) mma_commit(b_v_empty[vs]);
-          __syncwarp();
-          prev_ks = ks;
-          ++it;
-        }
-      }
-      if (!ok) break;
-      if (prev_ks >= 0) {
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (ok && !flush_dq(x)) {
-            fail();
-            ok = false;
-          }
-        }
-        if (!ok) break;
-        if (elected) mma_commit(b_k_empty[prev_ks]);
-        __syncwarp();
-      }
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (ok && first_dq[x] && unit_count > 0 &&
-            !mbar_wait_warp(b_dq_free[x], (unit_count - 1) & 1, tmo, abort_flag)) {
-          fail();
-          ok = false;
-        }
-      }
-      if (!ok) break;
-      if (elected) {
-        mma_commit(b_dq_full[0]);
-        mma_commit(b_dq_full[1]);
-        mma_commit(b_q_empty);
-      }
-      __syncwarp();
-    }
-    if (elected) mma_commit(b_drain);
-    __syncwarp();
-    mbar_wait_warp(b_drain, 0, tmo, nullptr);
-  } else {
-    // ------------------------------------------------------------ compute
-    const int x = warp >> 2;
-    const int quad = warp & 3;
-    const int t = quad * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tSP = tmem + lane_base + L::col_sp(x);
-    const uint32_t tDQ = tmem + lane_base + L::col_dq(x);
-    const float c_log2 = args.scale_log2;
-    uint32_t s_cnt = 0, dp_cnt = 0;
-    bool ok = true;
-    int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
-      int bh, b, qt0;
-      unit_coords(u, bh, b, qt0);
-      const int qt = qt0 + x;
-      const int row = qt * kTile + t;
-      const bool row_in = row < N;
-      const long long ridx = static_cast<long long>(bh) * N + row;
-      const float lse2 = lse2_of(args.lse, ridx, row_in);
-      const float dsum = row_in ? args.dsum[ridx] : 0.f;
-      const uint32_t row_global = static_cast<uint32_t>(ridx);
-      const int kv_len = kv_len_of(mk, b);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      int jmax = n_kv;
-      if (mk.causal && qt + 1 < jmax) jmax = qt + 1;
-      int n_done = 0;
-      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits(mk, qt, chunk, n_q, n_kv);
-        while (bits != 0u) {
-          const int j = chunk * 32 + (__ffs(bits) - 1);
-          bits &= bits - 1;
-          // dropout keep bits for keys [128 j, 128 j + 128) of this row
-          uint32_t zb[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
-          if constexpr (DROPOUT) {
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const uint4 kw =
-                  dropout_keep16(args.drop, row_global, static_cast<uint32_t>(j * 8 + g));
-              const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
-              uint32_t bits16 = 0;
-#pragma unroll
-              for (int e = 0; e < 16; ++e) bits16 |= ((w4[e >> 2] >> (8 * (e & 3))) & 1u) << e;
-              zb[g >> 1] = (g & 1) ? ((zb[g >> 1] & 0xFFFFu) | (bits16 << 16)) : bits16;
-            }
-          }
-          const bool emask = tile_needs_element_mask(mk, qt, j, kv_len);
-          int lim = kv_len - j * kTile;
-          if (mk.causal) {
-            const int lc = row - j * kTile + 1;
-            lim = lc < lim ? lc : lim;
-          }
-          // ---- phase 1: P, kept packed in registers
-          if (!mbar_wait_warp(b_s_full[x], s_cnt & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          ++s_cnt;
-          tc_fence_after();
-          uint32_t pp[64];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t sr[32];
-            tmem_ld32(tSP + 32 * c, sr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              float p0 = ex2_approx(fmaf(__uint_as_float(sr[k]), c_log2, -lse2));
-              float p1 = ex2_approx(fmaf(__uint_as_float(sr[k + 1]), c_log2, -lse2));
-              if (emask) {
-                p0 = (32 * c + k < lim) ? p0 : 0.f;
-                p1 = (32 * c + k + 1 < lim) ? p1 : 0.f;
-              }
-              pp[16 * c + k / 2] = pack_bf16x2(p0, p1);
-            }
-          }
-          tc_fence_before();
-          mbar_arrive(b_sp_free[x]);
-          // ---- phase 2: dS = P (Z dP / (1 - p) - D), written over dP as bf16
-          if (!mbar_wait_warp(b_dp_full[x], dp_cnt & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          ++dp_cnt;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t dr[32];
-            tmem_ld32(tSP + 32 * c, dr);
-            tmem_ld_wait();
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const float2 pf =
-                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * c + k / 2]));
-              float z0 = args.drop.keep_scale, z1 = args.drop.keep_scale;
-              if constexpr (DROPOUT) {
-                z0 = ((zb[c] >> k) & 1u) ? z0 : 0.f;
-                z1 = ((zb[c] >> (k + 1)) & 1u) ? z1 : 0.f;
-              }
-              const float ds0 = pf.x * fmaf(z0, __uint_as_float(dr[k]), -dsum);
-              const float ds1 = pf.y * fmaf(z1, __uint_as_float(dr[k + 1]), -dsum);
-              pk[k / 2] = pack_bf16x2(ds0, ds1);
-            }
-            tmem_st16(tSP + 16 * c, pk);
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(b_ds_ready[x]);
-          ++n_done;
-        }
-      }
-      if (!ok) break;
-      // ---- epilogue: dQ = scale * acc
-      if (!mbar_wait_warp(b_dq_full[x], unit_count & 1, tmo, abort_flag)) {
-        fail();
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      __nv_bfloat16* dst = args.dq + static_cast<size_t>(ridx) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        if (n_done > 0) {
-          tmem_ld32(tDQ + 32 * c, v);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          pk[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * args.scale,
-                              __uint_as_float(v[2 * k + 1]) * args.scale);
-        if (row_in) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(b_dq_free[x]);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
 template <typename K>
 cudaError_t set_smem(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1118,17 +601,6 @@ static cudaError_t launch_dkdv_impl(const CUtensorMap& tq, const CUtensorMap& tk
   return cudaGetLastError();
 }
 
-template <int D, bool DROP>
-static cudaError_t launch_dq_impl(const CUtensorMap& tq, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
-                                  int grid, cudaStream_t stream) {
-  auto kern = fa_bwd_dq_kernel<D, DROP>;
-  cudaError_t e = set_smem(kern, DqLayout<D>::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kBwdThreads, DqLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, int d, bool dropout,
                             int num_sms, cudaStream_t stream) {
@@ -1144,13 +616,7 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, int d, bool dropout,
                           int num_sms, cudaStream_t stream) {
-  const int n_q = (a.mask.N + kTile - 1) / kTile;
-  const long long units = static_cast<long long>(a.mask.B) * a.mask.H * ((n_q + 1) / 2);
-  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  if (grid <= 0) return cudaSuccess;
   return launch_bwd_dq_split(tq, tk, tv, tdo, a, d, dropout, num_sms, stream);
-  return dropout ? launch_dq_impl<128, true>(tq, tk, tv, tdo, a, grid, stream)
-                 : launch_dq_impl<128, false>(tq, tk, tv, tdo, a, grid, stream);
 }
 
 }  // namespace fa

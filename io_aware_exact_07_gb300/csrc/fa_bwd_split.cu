@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, q_arms = 0, kv_arms[2] = {0, 0};
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const int bh = u / n_t, kt = u % n_t;
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const int bh = u / n_t, kt = u % n_t;
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, prc = 0, dsc = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const int bh = u / n_t, kt = u % n_t;
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, gt = 0, stc = 0, dpc = 0, pdc = 0, dsc = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const int bh = u / n_t, kt = u % n_t;
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -719,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, k_arms = 0, v_arms = 0, qd_arms[2] = {0, 0};
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       int bh, qt;
       unit_coords(u, bh, qt);
       const int kv_len = kv_len_of(mk, bh / mk.H);
@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       int bh, qt;
       unit_coords(u, bh, qt);
       const int kv_len = kv_len_of(mk, bh / mk.H);
@@ -840,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, dsc = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       int bh, qt;
       unit_coords(u, bh, qt);
       const int kv_len = kv_len_of(mk, bh / mk.H);
@@ -904,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gt = 0, sc = 0, dc = 0, ddc = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       int bh, qt;
       unit_coords(u, bh, qt);
       const int row = qt * kTile + t;

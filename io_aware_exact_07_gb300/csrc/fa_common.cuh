@@ -48,6 +48,20 @@ __device__ __forceinline__ int kv_len_of(const MaskParams& m, int b) {
   return L < 0 ? 0 : (L > m.N ? m.N : L);
 }
 
+// Static schedule of the persistent kernels: in round k the CTAs take the
+// positions [k G, k G + G) of the work list, G = gridDim.x, in forward order
+// on even rounds and in reverse order on odd rounds. Every role of a CTA walks
+// the same sequence. With a causal mask the work list is ordered longest unit
+// first within each head, so a CTA that drew a long unit in one round draws a
+// short one in the next and the per-CTA totals stay within a few percent of
+// each other; head-major order keeps the CTAs of a round on a few heads, whose
+// K/V tiles they then share in L2. Returns a position >= the list length once
+// the CTA has no more work (positions grow with k).
+__device__ __forceinline__ int sched_unit(int k) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
 // Whether the (query tile qt, key tile kt) pair has any allowed element.
 // n_kv = ceil(kv_len / 128), n_q = ceil(N / 128).
 __device__ __forceinline__ bool tile_valid(const MaskParams& m, int qt, int kt, int n_q,

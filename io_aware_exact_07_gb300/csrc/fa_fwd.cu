@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tm_v);
     }
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
       const int kv_len = kv_len_of(mk, uc.b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                (first && kk == 0) ? 0u : 1u);
     };
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
       const int kv_len = kv_len_of(mk, uc.b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t it = 0, p_cnt0 = 0, p_cnt1 = 0;
       bool ok = true;
       int unit_count = 0;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
         const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
         const int kv_len = kv_len_of(mk, uc.b);
         const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint32_t pv_cnt = 0;  // decoupled schedule: PV completions consumed
     bool ok = true;
     int unit_count = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++unit_count) {
+    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
       const int qt = uc.qt0 + x;
       const int row = qt * kTile + t;
