@@ -587,16 +587,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int k = 0; k < 128; ++k)
               if (k >= lim) s[k] = -INFINITY;
           }
-          float mx[16];
+          // Row maximum: three-input max over eight independent accumulators.
+          float mx[8];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) mx[k] = s[k];
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
 #pragma unroll
-          for (int k = 16; k < 128; ++k) mx[k & 15] = fmaxf(mx[k & 15], s[k]);
+          for (int k = 16; k < 128; k += 16)
 #pragma unroll
-          for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
-          const float m_tile = mx[0] * c_log2;
+            for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], s[k + 2 * a], s[k + 2 * a + 1]);
+          const float mx_row = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                     fmaxf(mx[6], mx[7]));
+          const float m_tile = mx_row * c_log2;
           const float m_new = fmaxf(m_ref, m_tile);
           const bool grow = m_new > m_ref + kRescaleThreshold;
           float alpha = 1.f;
@@ -607,8 +608,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           // P = exp2(s*c - m_ref), summed (undropped) into l, dropout applied,
-          // packed to bf16 and stored over S, 64 columns at a time.
-          float rs0 = 0.f, rs1 = 0.f;
+          // packed to bf16 and stored over S, 64 columns at a time. The scale
+          // and subtract and the row sum run on packed pairs of lanes.
+          const uint64_t c2 = f2_pack(c_log2, c_log2);
+          const uint64_t nm2 = f2_pack(-m_use, -m_use);
+          uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums
           uint32_t pk[64];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
@@ -626,10 +630,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               }
 #pragma unroll
               for (int e = 0; e < 16; e += 2) {
-                float p0 = ex2_approx(fmaf(s[k0 + e], c_log2, -m_use));
-                float p1 = ex2_approx(fmaf(s[k0 + e + 1], c_log2, -m_use));
-                rs0 += p0;
-                rs1 += p1;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s[k0 + e], s[k0 + e + 1]), c2, nm2), x0, x1);
+                float p0 = ex2_approx(x0);
+                float p1 = ex2_approx(x1);
+                rs2[(e >> 1) & 3] = f2_add(rs2[(e >> 1) & 3], f2_pack(p0, p1));
                 if constexpr (DROPOUT) {
                   p0 = ((w[e >> 2] >> (8 * (e & 3))) & 0xFFu) ? p0 : 0.f;
                   p1 = ((w[(e + 1) >> 2] >> (8 * ((e + 1) & 3))) & 0xFFu) ? p1 : 0.f;
@@ -639,7 +644,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
             if constexpr (!L::kSepP) tmem_st32(tS + half * 32, &pk[half * 32]);
           }
-          l_sum += rs0 + rs1;
+          {
+            const uint64_t t2 = f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3]));
+            float r0, r1;
+            f2_unpack(t2, r0, r1);
+            l_sum += r0 + r1;
+          }
           if constexpr (L::kSepP) {
             // The previous PV reads the P buffer and accumulates into O: wait for it.
             if (n_done > 0) {
