@@ -225,9 +225,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int row = qt * kTile + 4 * lane + r;
             const bool in = row < N;
             const long long idx = static_cast<long long>(bh) * N + row;
-            lp[r] = lse2_of(args.lse, idx, in);
-            dp[r] = in ? args.dsum[idx] : 0.f;
+            lp[r] = -lse2_of(args.lse, idx, in);
+            dp[r] = in ? -args.dsum[idx] : 0.f;
           }
+          // staged negated: the compute warps add them as packed pairs
           reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
           reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
           if (lane == 0) {
@@ -445,13 +446,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_ld32(tSt, &sr[0]);
             tmem_ld32(tSt + 32, &sr[32]);
             tmem_ld_wait();
+            const uint64_t c2 = f2_pack(c_log2, c_log2);
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
-              const float4 l4 = reinterpret_cast<const float4*>(lse_t)[c4];
-              p[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 0]), c_log2, -l4.x));
-              p[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 1]), c_log2, -l4.y));
-              p[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 2]), c_log2, -l4.z));
-              p[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 3]), c_log2, -l4.w));
+              const ulonglong2 nl = reinterpret_cast<const ulonglong2*>(lse_t)[c4];  // -lse2 pairs
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int c = 4 * c4 + 2 * h;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2,
+                                 h ? nl.y : nl.x),
+                          x0, x1);
+                p[c] = ex2_approx(x0);
+                p[c + 1] = ex2_approx(x1);
+              }
             }
           }
           if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
@@ -497,21 +505,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               tmem_ld_wait();
 #pragma unroll
               for (int c4 = 0; c4 < 8; ++c4) {
-                const float4 d4 = reinterpret_cast<const float4*>(dsum_t)[8 * h + c4];
-                const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                float ds[4];
+                const ulonglong2 nd = reinterpret_cast<const ulonglong2*>(dsum_t)[8 * h + c4];  // -D
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < 4; e += 2) {
                   const int c = 32 * h + 4 * c4 + e;
-                  float z = args.drop.keep_scale;
+                  float z0 = args.drop.keep_scale, z1 = args.drop.keep_scale;
                   if constexpr (DROPOUT) {
                     const uint32_t zw = (c < 32) ? zb0 : zb1;
-                    z = ((zw >> (c & 31)) & 1u) ? z : 0.f;
+                    z0 = ((zw >> (c & 31)) & 1u) ? z0 : 0.f;
+                    z1 = ((zw >> ((c + 1) & 31)) & 1u) ? z1 : 0.f;
                   }
-                  ds[e] = p[c] * fmaf(z, __uint_as_float(dr[4 * c4 + e]), -dv4[e]);
+                  const uint64_t t = f2_fma(f2_pack(z0, z1),
+                                            f2_pack(__uint_as_float(dr[4 * c4 + e]),
+                                                    __uint_as_float(dr[4 * c4 + e + 1])),
+                                            e ? nd.y : nd.x);
+                  float a0, a1;
+                  f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), a0, a1);
+                  pk[16 * h + 2 * c4 + (e >> 1)] = pack_bf16x2(a0, a1);
                 }
-                pk[16 * h + 2 * c4] = pack_bf16x2(ds[0], ds[1]);
-                pk[16 * h + 2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
               }
             }
             tmem_st32(tDPt, pk);

@@ -235,9 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = qt * kTile + 4 * lane + r;
             const bool in = row < N;
             const long long idx = static_cast<long long>(bh) * N + row;
-            lp[r] = lse2_at(args.lse, idx, in);
-            dp[r] = in ? args.dsum[idx] : 0.f;
+            lp[r] = -lse2_at(args.lse, idx, in);
+            dp[r] = in ? -args.dsum[idx] : 0.f;
           }
+          // staged negated: the compute warps add them as packed pairs
           reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
           reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
           if (lane == 0) {
@@ -450,13 +451,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_before();
               mbar_arrive(bars.st_free);
             }
+            const uint64_t c2 = f2_pack(c_log2, c_log2);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 l4 = reinterpret_cast<const float4*>(lse_t)[c4];
-              p[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 0]), c_log2, -l4.x));
-              p[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 1]), c_log2, -l4.y));
-              p[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 2]), c_log2, -l4.z));
-              p[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(sr[4 * c4 + 3]), c_log2, -l4.w));
+              const ulonglong2 nl = reinterpret_cast<const ulonglong2*>(lse_t)[c4];  // -lse2 pairs
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int c = 4 * c4 + 2 * h;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2,
+                                 h ? nl.y : nl.x),
+                          x0, x1);
+                p[c] = ex2_approx(x0);
+                p[c + 1] = ex2_approx(x1);
+              }
             }
           }
           if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
@@ -506,17 +514,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 d4 = reinterpret_cast<const float4*>(dsum_t)[c4];
-              const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-              float ds[4];
+              const ulonglong2 nd = reinterpret_cast<const ulonglong2*>(dsum_t)[c4];  // -D pairs
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int c = 4 * c4 + e;
-                const float z = ((zb >> c) & 1u) ? args.drop.keep_scale : 0.f;
-                ds[e] = p[c] * fmaf(z, __uint_as_float(dr[c]), -dv4[e]);
+              for (int h = 0; h < 2; ++h) {
+                const int c = 4 * c4 + 2 * h;
+                const float z0 = ((zb >> c) & 1u) ? args.drop.keep_scale : 0.f;
+                const float z1 = ((zb >> (c + 1)) & 1u) ? args.drop.keep_scale : 0.f;
+                const uint64_t t = f2_fma(f2_pack(z0, z1),
+                                          f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
+                                          h ? nd.y : nd.x);
+                float a0, a1;
+                f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), a0, a1);
+                pk[2 * c4 + h] = pack_bf16x2(a0, a1);
               }
-              pk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-              pk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
             }
             if constexpr (L::kSepBuf) {
               if (gt > 0) {  // the previous dK has finished reading the dS^T buffer
@@ -912,6 +922,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long ridx = static_cast<long long>(bh) * N + row;
       const float lse2 = lse2_at(args.lse, ridx, row_in);
       const float dsum = row_in ? args.dsum[ridx] : 0.f;
+      const uint64_t c2 = f2_pack(c_log2, c_log2);
+      const uint64_t nl2 = f2_pack(-lse2, -lse2);
+      const uint64_t nd2 = f2_pack(-dsum, -dsum);
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int jmax = kv_limit(qt, n_kv);
@@ -934,15 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 zb |= ((w4[e >> 2] >> (8 * (e & 3))) & 1u) << (16 * g + e);
             }
           }
-          int lim = 128;  // keys [0, lim) of this tile are allowed for this row
-          if (tile_needs_element_mask(mk, qt, j, kv_len)) {
-            lim = kv_len - j * kTile;
-            if (mk.causal) {
-              const int lc = row - j * kTile + 1;
-              lim = lc < lim ? lc : lim;
-            }
-          }
-          const int lim_local = lim - 32 * wg;
+          const bool masked = tile_needs_element_mask(mk, qt, j, kv_len);
           // ---- P = exp2(S c - lse2), kept as bf16 pairs
           if (!mbar_wait_warp(bars.s_full, sc++ & 1, tmo, abort_flag)) {
             fail();
@@ -958,9 +963,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(bars.s_free);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float e = ex2_approx(fmaf(__uint_as_float(sr[c]), c_log2, -lse2));
-              p[c] = (c < lim_local) ? e : 0.f;
+            for (int c = 0; c < 32; c += 2) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2,
+                               nl2),
+                        x0, x1);
+              p[c] = ex2_approx(x0);
+              p[c + 1] = ex2_approx(x1);
+            }
+            if (masked) {  // keys [0, lim) of this tile are allowed for this row
+              int lim = kv_len - j * kTile;
+              if (mk.causal) {
+                const int lc = row - j * kTile + 1;
+                lim = lc < lim ? lc : lim;
+              }
+              const int lim_local = lim - 32 * wg;
+#pragma unroll
+              for (int c = 0; c < 32; ++c) p[c] = (c < lim_local) ? p[c] : 0.f;
             }
           }
           // ---- dS = P (Z dP / (1 - p) - D)
@@ -981,8 +1000,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 16; ++c) {
               const float z0 = ((zb >> (2 * c)) & 1u) ? args.drop.keep_scale : 0.f;
               const float z1 = ((zb >> (2 * c + 1)) & 1u) ? args.drop.keep_scale : 0.f;
-              const float d0 = p[2 * c] * fmaf(z0, __uint_as_float(dr[2 * c]), -dsum);
-              const float d1 = p[2 * c + 1] * fmaf(z1, __uint_as_float(dr[2 * c + 1]), -dsum);
+              const uint64_t t = f2_fma(f2_pack(z0, z1),
+                                        f2_pack(__uint_as_float(dr[2 * c]),
+                                                __uint_as_float(dr[2 * c + 1])),
+                                        nd2);
+              float d0, d1;
+              f2_unpack(f2_mul(f2_pack(p[2 * c], p[2 * c + 1]), t), d0, d1);
               pk[c] = pack_bf16x2(d0, d1);
             }
           }
