@@ -912,6 +912,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tDQ = tmem + lane_base + L::kColDQ + kQCols * wg;
     const float c_log2 = args.scale_log2;
     uint32_t gt = 0, sc = 0, dc = 0, ddc = 0;
+    // At d = 128 the dS store's completion is waited for under the next step's
+    // S load (measured faster); at d = 64 the dQ MMA must not wait for it
+    // (measured slower), so the store is completed at once.
+    constexpr bool kDeferDs = (D == 128);
+    bool ds_pending = false;  // a dS store issued whose ds_ready arrival is still due
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
@@ -959,6 +964,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           {
             uint32_t sr[32];
             tmem_ld32(tS, sr);
+            if (kDeferDs && ds_pending) {  // the previous step's dS store completes under this load
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(bars.ds_ready);
+              ds_pending = false;
+            }
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(bars.s_free);
@@ -1018,14 +1029,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
           tmem_st16(tDS, pk);
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(bars.ds_ready);
+          if constexpr (kDeferDs) {
+            ds_pending = true;  // completed, and ds_ready arrived, under the next S load
+          } else {
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bars.ds_ready);
+          }
           ++n_done;
           ++gt;
         }
       }
       if (!ok) break;
+      if (ds_pending) {  // the last dQ MMA of the unit needs this step's dS
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bars.ds_ready);
+        ds_pending = false;
+      }
       // ---- epilogue: dQ = scale * acc, D/4 columns per warpgroup
       if (!mbar_wait_warp(bars.dq_full, unit_count & 1, tmo, abort_flag)) {
         fail();
@@ -1056,6 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bars.dq_free);
     }
+    tmem_st_wait();  // no tensor-memory store may still be in flight on any exit path
   }
   tc_fence_before();
   __syncthreads();
