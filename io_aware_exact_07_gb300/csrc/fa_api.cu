@@ -127,6 +127,12 @@ fa::DropParams make_drop(float p, uint64_t seed, uint64_t offset) {
   d.seed_hi = static_cast<uint32_t>(seed >> 32);
   d.off_lo = static_cast<uint32_t>(offset);
   d.off_hi = static_cast<uint32_t>(offset >> 32);
+  // Philox4x32 key schedule (Salmon et al., SC'11): the key grows by the two
+  // Weyl constants every round.
+  for (int r = 0; r < 10; ++r) {
+    d.rk_lo[r] = d.seed_lo + static_cast<uint32_t>(r) * 0x9E3779B9u;
+    d.rk_hi[r] = d.seed_hi + static_cast<uint32_t>(r) * 0xBB67AE85u;
+  }
   return d;
 }
 

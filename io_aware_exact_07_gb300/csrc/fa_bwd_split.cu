@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tP = tmem + lane_base + L::kColP + L::kPair * wg;
     const uint32_t tDS = tmem + lane_base + L::kColDS + L::kPair * wg;
     const float c_log2 = args.scale_log2;
+    const uint64_t ks2 = f2_pack(args.drop.keep_scale, args.drop.keep_scale);
     uint32_t* drop_scratch = reinterpret_cast<uint32_t*>(smem + L::kDropOff + warp * 1024);
     uint32_t it = 0, gt = 0, stc = 0, dpc = 0, pdc = 0, dsc = 0;
     bool ok = true;
@@ -411,7 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* lse_t = lse_s + s * 128 + 32 * wg;
           const float* dsum_t = dsum_s + s * 128 + 32 * wg;
           const int q0 = qt * kTile + 32 * wg;  // first query column of this warpgroup
-          uint32_t zb = 0xFFFFFFFFu;            // dropout keep bit per query column
+          // Dropout keep bytes (0x00 / 0xFF) of this thread's key for the 32 query
+          // columns, four per word: column c is byte c & 3 of bm[c >> 2].
+          uint32_t bm[8];
           if constexpr (DROPOUT) {
             // The warp's 32 keys are two 16-key Philox groups; for each of the 32
             // queries both groups are generated (two blocks per lane) and each
@@ -427,11 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                   dropout_keep16(args.drop, rowg, kgroup0 + gs);
             }
             __syncwarp();
-            zb = 0u;
+            // this lane's key is byte (lane & 3) of word (lane & 15) >> 2 of the
+            // block of its 16-key group: gather it for four columns at a time
+            const uint32_t kb = static_cast<uint32_t>(lane & 3);
+            const uint32_t sel2 = kb | ((4u + kb) << 4);  // byte kb of a, then byte kb of b
+            const uint32_t* wcol = drop_scratch + (lane >> 4) * 4 + ((lane & 15) >> 2);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const uint32_t w = drop_scratch[(c * 2 + (lane >> 4)) * 4 + ((lane & 15) >> 2)];
-              zb |= ((w >> (8 * (lane & 3))) & 1u) << c;  // bytes are 0x00 or 0xFF
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t t0 = prmt(wcol[(4 * k + 0) * 8], wcol[(4 * k + 1) * 8], sel2);
+              const uint32_t t1 = prmt(wcol[(4 * k + 2) * 8], wcol[(4 * k + 3) * 8], sel2);
+              bm[k] = prmt(t0, t1, 0x5410u);
             }
             __syncwarp();
           }
@@ -477,9 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[16];  // dropped copy for dV
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const float a0 = ((zb >> (2 * c)) & 1u) ? p[2 * c] : 0.f;
-              const float a1 = ((zb >> (2 * c + 1)) & 1u) ? p[2 * c + 1] : 0.f;
-              pk[c] = pack_bf16x2(a0, a1);
+              uint32_t pp = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+              if constexpr (DROPOUT) pp &= prmt(bm[c >> 1], 0u, (c & 1) ? 0x3322u : 0x1100u);
+              pk[c] = pp;
             }
             if constexpr (L::kSepBuf) {
               if (gt > 0) {  // the previous dV has finished reading the P^T buffer
@@ -518,10 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 const int c = 4 * c4 + 2 * h;
-                const float z0 = ((zb >> c) & 1u) ? args.drop.keep_scale : 0.f;
-                const float z1 = ((zb >> (c + 1)) & 1u) ? args.drop.keep_scale : 0.f;
-                const uint64_t t = f2_fma(f2_pack(z0, z1),
-                                          f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
+                uint32_t dp0 = dr[c], dp1 = dr[c + 1];
+                if constexpr (DROPOUT) {  // keep byte -> all-ones / all-zeros lane mask
+                  dp0 &= prmt(bm[c >> 2], 0u, (8u | (c & 3)) * 0x1111u);
+                  dp1 &= prmt(bm[c >> 2], 0u, (8u | ((c + 1) & 3)) * 0x1111u);
+                }
+                const uint64_t t = f2_fma(ks2, f2_pack(__uint_as_float(dp0), __uint_as_float(dp1)),
                                           h ? nd.y : nd.x);
                 float a0, a1;
                 f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), a0, a1);
@@ -930,6 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t c2 = f2_pack(c_log2, c_log2);
       const uint64_t nl2 = f2_pack(-lse2, -lse2);
       const uint64_t nd2 = f2_pack(-dsum, -dsum);
+      const uint64_t ks2 = f2_pack(args.drop.keep_scale, args.drop.keep_scale);
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int jmax = kv_limit(qt, n_kv);
@@ -939,17 +950,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (bits != 0u && ok) {
           const int j = chunk * 32 + (__ffs(bits) - 1);
           bits &= bits - 1;
-          uint32_t zb = 0xFFFFFFFFu;  // dropout keep bit per key column
+          // Dropout keep bytes (0x00 / 0xFF) of this row's 32 key columns, four
+          // per word: column c is byte c & 3 of word c >> 2.
+          uint32_t kb[8];
           if constexpr (DROPOUT) {
-            zb = 0u;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
               const uint4 kw = dropout_keep16(args.drop, static_cast<uint32_t>(ridx),
                                               static_cast<uint32_t>(j * 8 + 2 * wg + g));
-              const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                zb |= ((w4[e >> 2] >> (8 * (e & 3))) & 1u) << (16 * g + e);
+              kb[4 * g + 0] = kw.x;
+              kb[4 * g + 1] = kw.y;
+              kb[4 * g + 2] = kw.z;
+              kb[4 * g + 3] = kw.w;
             }
           }
           const bool masked = tile_needs_element_mask(mk, qt, j, kv_len);
@@ -1009,12 +1021,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(bars.dp_free);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const float z0 = ((zb >> (2 * c)) & 1u) ? args.drop.keep_scale : 0.f;
-              const float z1 = ((zb >> (2 * c + 1)) & 1u) ? args.drop.keep_scale : 0.f;
-              const uint64_t t = f2_fma(f2_pack(z0, z1),
-                                        f2_pack(__uint_as_float(dr[2 * c]),
-                                                __uint_as_float(dr[2 * c + 1])),
-                                        nd2);
+              uint32_t dp0 = dr[2 * c], dp1 = dr[2 * c + 1];
+              if constexpr (DROPOUT) {
+                // keep byte -> all-ones / all-zeros lane mask (sign replicated)
+                const uint32_t wd = kb[c >> 1];
+                const uint32_t b0 = (2 * c) & 3;
+                dp0 &= prmt(wd, 0u, (8u | b0) * 0x1111u);
+                dp1 &= prmt(wd, 0u, (8u | (b0 + 1u)) * 0x1111u);
+              }
+              const uint64_t t =
+                  f2_fma(ks2, f2_pack(__uint_as_float(dp0), __uint_as_float(dp1)), nd2);
               float d0, d1;
               f2_unpack(f2_mul(f2_pack(p[2 * c], p[2 * c + 1]), t), d0, d1);
               pk[c] = pack_bf16x2(d0, d1);

@@ -29,6 +29,10 @@ struct DropParams {
   int p8;                       // drop iff Philox byte < p8
   float keep_scale;             // 1 / (1 - p8 / 256)
   uint32_t seed_lo, seed_hi, off_lo, off_hi;
+  // Philox round keys, (seed_lo + r W0, seed_hi + r W1) mod 2^32 for rounds
+  // r = 0..9, filled on the host so that a kernel reads them as constant
+  // operands instead of bumping the key every round.
+  uint32_t rk_lo[10], rk_hi[10];
 };
 
 struct SyncParams {
@@ -118,16 +122,37 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// The same generator with the round keys taken from DropParams.
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const DropParams& d) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ d.rk_lo[r], lo1, hi0 ^ c.w ^ d.rk_hi[r], lo0);
+  }
+  return c;
+}
+
 // Keep masks for the 16 keys [16*g, 16*g + 16) of query row `row_global`
 // ((b*H + h)*N + i): each byte is 0xFF where the element is kept, 0 where dropped.
 __device__ __forceinline__ uint4 dropout_keep16(const DropParams& d, uint32_t row_global,
                                                 uint32_t key_group) {
-  const uint4 r = philox4x32_10(make_uint4(key_group, row_global, d.off_lo, d.off_hi), d.seed_lo,
-                                d.seed_hi);
+  const uint4 r = philox4x32_10_rk(make_uint4(key_group, row_global, d.off_lo, d.off_hi), d);
   const uint32_t thr = static_cast<uint32_t>(d.p8) * 0x01010101u;
   // per-byte unsigned compare: 0xFF where byte >= p8
   return make_uint4(__vcmpgeu4(r.x, thr), __vcmpgeu4(r.y, thr), __vcmpgeu4(r.z, thr),
                     __vcmpgeu4(r.w, thr));
+}
+
+// Byte permute: result byte i = byte sel.nibble[i] of the 8-byte value {b, a}
+// (a = bytes 0-3); a nibble with bit 3 set replicates that byte's sign bit.
+// Used to turn dropout keep bytes (0x00 / 0xFF) into lane masks.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
 }
 
 // bf16x2 helpers for the epilogues.

@@ -635,11 +635,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 float p0 = ex2_approx(x0);
                 float p1 = ex2_approx(x1);
                 rs2[(e >> 1) & 3] = f2_add(rs2[(e >> 1) & 3], f2_pack(p0, p1));
-                if constexpr (DROPOUT) {
-                  p0 = ((w[e >> 2] >> (8 * (e & 3))) & 0xFFu) ? p0 : 0.f;
-                  p1 = ((w[(e + 1) >> 2] >> (8 * ((e + 1) & 3))) & 0xFFu) ? p1 : 0.f;
-                }
-                pk[half * 32 + g * 8 + (e >> 1)] = pack_bf16x2(p0, p1);
+                uint32_t pp = pack_bf16x2(p0, p1);
+                // dropout: keep bytes e, e+1 (0x00 / 0xFF) widened to the two bf16 lanes
+                if constexpr (DROPOUT) pp &= prmt(w[e >> 2], 0u, (e & 2) ? 0x3322u : 0x1100u);
+                pk[half * 32 + g * 8 + (e >> 1)] = pp;
               }
             }
             if constexpr (!L::kSepP) tmem_st32(tS + half * 32, &pk[half * 32]);
