@@ -38,6 +38,11 @@ struct TileT {
   static constexpr int kChunks = D / 64;  // 64-column (128-byte swizzle) chunks of 16 KB
 };
 
+// Barrier arrays are sized for the deepest ring of either head size.
+constexpr int kMaxQStages = 3;  // dK/dV kernel: Q / dO ring
+constexpr int kMaxKStages = 4;  // dQ kernel: K ring
+constexpr int kMaxVStages = 3;  // dQ kernel: V ring
+
 __device__ __forceinline__ float lse2_at(const float* lse, long long idx, bool in_range) {
   if (!in_range) return INFINITY;
   const float l = lse[idx];
@@ -84,6 +89,7 @@ struct DkdvL {
   static constexpr bool kSepBuf = (D == 64);       // separate P^T / dS^T buffers
   static constexpr int kKVBufs = (D == 64) ? 2 : 1;
   static constexpr int kStages = (D == 64) ? 3 : 2;
+  static_assert(kStages <= kMaxQStages, "Q / dO ring deeper than its barrier arrays");
   static constexpr int kKVOff = 0;                                   // kKVBufs x (K, V)
   static constexpr int kQOff = kKVBufs * 2 * T;
   static constexpr int kDOOff = kQOff + kStages * T;
@@ -91,7 +97,7 @@ struct DkdvL {
   static constexpr int kDsumOff = kLseOff + kStages * 512;
   static constexpr int kDropOff = kDsumOff + kStages * 512;          // 16 warps x 1 KB
   static constexpr int kBarOff = kDropOff + kComputeWarps * 1024;
-  static constexpr int kNumBars = 4 + 2 * 3 + 12;
+  static constexpr int kNumBars = 4 + 2 * kMaxQStages + 12;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColSt = 2 * D, kColDPt = 2 * D + 128;
@@ -101,7 +107,7 @@ struct DkdvL {
 };
 
 struct DkdvBars {
-  uint32_t kv_full[2], kv_empty[2], q_full[3], q_empty[3];
+  uint32_t kv_full[2], kv_empty[2], q_full[kMaxQStages], q_empty[kMaxQStages];
   uint32_t st_full, st_free, dpt_full, dpt_free, p_ready, p_done, ds_ready, ds_done;
   uint32_t acc_full, acc_free, drain_a, drain_b;
 };
@@ -137,8 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
     for (int b = 0; b < 2; ++b) bars.kv_full[b] = nb();
     for (int b = 0; b < 2; ++b) bars.kv_empty[b] = nb();
-    for (int s = 0; s < 3; ++s) bars.q_full[s] = nb();
-    for (int s = 0; s < 3; ++s) bars.q_empty[s] = nb();
+    for (int s = 0; s < kMaxQStages; ++s) bars.q_full[s] = nb();
+    for (int s = 0; s < kMaxQStages; ++s) bars.q_empty[s] = nb();
     bars.st_full = nb();
     bars.st_free = nb();
     bars.dpt_full = nb();
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.kv_full[b], 1);
       mbar_init(bars.kv_empty[b], 1);
     }
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < kMaxQStages; ++s) {
       mbar_init(bars.q_full[s], 32);
       mbar_init(bars.q_empty[s], 2 + kComputeWarps);  // both issuers + every compute warp
     }
@@ -620,18 +626,21 @@ struct DqL {
   static constexpr int kQDBufs = (D == 64) ? 2 : 1;
   static constexpr int kKStages = (D == 64) ? 4 : 3;
   static constexpr int kVStages = (D == 64) ? 3 : 2;
+  static_assert(kKStages <= kMaxKStages && kVStages <= kMaxVStages,
+                "K / V ring deeper than its barrier arrays");
   static constexpr int kQOff = 0;                                  // kQDBufs x (Q, dO)
   static constexpr int kKOff = kQDBufs * 2 * T;
   static constexpr int kVOff = kKOff + kKStages * T;
   static constexpr int kBarOff = kVOff + kVStages * T;
-  static constexpr int kNumBars = 4 + 2 * 4 + 2 * 3 + 10;
+  static constexpr int kNumBars = 4 + 2 * kMaxKStages + 2 * kMaxVStages + 10;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
 };
 
 struct DqBars {
-  uint32_t qd_full[2], qd_empty[2], k_full[4], k_empty[4], v_full[3], v_empty[3];
+  uint32_t qd_full[2], qd_empty[2], k_full[kMaxKStages], k_empty[kMaxKStages];
+  uint32_t v_full[kMaxVStages], v_empty[kMaxVStages];
   uint32_t s_full, s_free, dp_full, dp_free, ds_ready, ds_done, dq_full, dq_free;
   uint32_t drain_a, drain_b;
 };
@@ -665,10 +674,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
     for (int b = 0; b < 2; ++b) bars.qd_full[b] = nb();
     for (int b = 0; b < 2; ++b) bars.qd_empty[b] = nb();
-    for (int s = 0; s < 4; ++s) bars.k_full[s] = nb();
-    for (int s = 0; s < 4; ++s) bars.k_empty[s] = nb();
-    for (int s = 0; s < 3; ++s) bars.v_full[s] = nb();
-    for (int s = 0; s < 3; ++s) bars.v_empty[s] = nb();
+    for (int s = 0; s < kMaxKStages; ++s) bars.k_full[s] = nb();
+    for (int s = 0; s < kMaxKStages; ++s) bars.k_empty[s] = nb();
+    for (int s = 0; s < kMaxVStages; ++s) bars.v_full[s] = nb();
+    for (int s = 0; s < kMaxVStages; ++s) bars.v_empty[s] = nb();
     bars.s_full = nb();
     bars.s_free = nb();
     bars.dp_full = nb();
@@ -686,11 +695,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.qd_full[b], 1);
       mbar_init(bars.qd_empty[b], 1);
     }
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < kMaxKStages; ++s) {
       mbar_init(bars.k_full[s], 1);
       mbar_init(bars.k_empty[s], 1);
     }
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < kMaxVStages; ++s) {
       mbar_init(bars.v_full[s], 1);
       mbar_init(bars.v_empty[s], 1);
     }

@@ -46,6 +46,7 @@ struct FwdLayout {
   static constexpr int kChunks = D / 64;                 // 64-column (128-byte) swizzle chunks
   static constexpr int kTileBytes = kTile * D * 2;       // one 128 x D bf16 tile
   static constexpr int kStages = (D == 64) ? 4 : 2;      // K/V ring depth
+  static_assert(kStages <= 4, "the K/V ring's barrier arrays hold four stages");
   static constexpr int kQOff = 0;                        // Q_a, Q_b
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
