@@ -202,3 +202,35 @@ def bwd(q, k, v, dout, scale, causal=False, dropout_p=0.0, seed=0, offset=0, blo
         dq, dk, dv = (x.reshape(shape4[0], shape4[1], N, d) for x in (dq, dk, dv))
         D = D.reshape(shape4[0], shape4[1], N)
     return dq, dk, dv, D
+
+
+def _group(H: int, Hkv: int) -> int:
+    if Hkv < 1 or H % Hkv != 0:
+        raise ValueError(f"H={H} is not a multiple of H_kv={Hkv}")
+    return H // Hkv
+
+
+def fwd_gqa(q, k, v, scale, **kw):
+    """Grouped-query attention forward (the K/V-head sharing the cross-paper
+    synthesis page lists among FlashAttention's successors): q [B, H, N, d],
+    k and v [B, H_kv, N, d] with H a multiple of H_kv; query head h of batch b
+    attends with K/V head h // (H / H_kv). Written out from that definition:
+    every query head gets its group's K/V and the per-head forward above runs
+    unchanged (dropout keyed by the query head, as for H independent heads)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    G = _group(q.shape[1], k.shape[1])
+    return fwd(q, np.repeat(k, G, axis=1), np.repeat(v, G, axis=1), scale, **kw)
+
+
+def bwd_gqa(q, k, v, dout, scale, **kw):
+    """Backward of fwd_gqa: dq per query head; dk and dv of a K/V head are the
+    sums over the G query heads that share it (each of them used that K/V).
+    Returns (dq [B, H, N, d], dk [B, H_kv, N, d], dv [B, H_kv, N, d], D)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    G = _group(H, Hkv)
+    dq, dk, dv, D = bwd(q, np.repeat(k, G, axis=1), np.repeat(v, G, axis=1), dout, scale, **kw)
+    dk = dk.reshape(B, Hkv, G, N, d).sum(axis=2)
+    dv = dv.reshape(B, Hkv, G, N, d).sum(axis=2)
+    return dq, dk, dv, D

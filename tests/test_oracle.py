@@ -381,3 +381,60 @@ def test_pages_worked_example_score_matrix_size():
     n_bytes = g["heads"] * g["seq_len"] ** 2 * g["bytes_per_element"]
     assert n_bytes == g["bytes"]
     assert abs(n_bytes / 2 ** 30 - g["approx_GiB"]) < 1e-9
+
+
+# ------------------------------------------------------- grouped-query heads
+
+def _loss_gqa(q, k, v, do, opts):
+    o, _ = oracle.fwd_gqa(q, k, v, opts["scale"], causal=opts["causal"], dropout_p=opts["p"],
+                          seed=3, offset=7)
+    return float((o * do).sum())
+
+
+@pytest.mark.parametrize("H,Hkv,causal,p", [(2, 1, False, 0.0), (4, 2, True, 0.0),
+                                            (3, 1, True, 0.25)])
+def test_gqa_backward_matches_finite_differences(H, Hkv, causal, p):
+    # dK / dV of a shared K/V head must be the sum over its query heads: a
+    # dropped sum or a wrong head map fails the finite-difference check.
+    N, d = 5, 2
+    r = rng(7 + H * 3 + Hkv)
+    q = r.standard_normal((1, H, N, d))
+    k = r.standard_normal((1, Hkv, N, d))
+    v = r.standard_normal((1, Hkv, N, d))
+    do = r.standard_normal((1, H, N, d))
+    opts = dict(scale=0.6, causal=causal, p=p)
+    dq, dk, dv, _ = oracle.bwd_gqa(q, k, v, do, opts["scale"], causal=causal, dropout_p=p,
+                                   seed=3, offset=7)
+    h = 1e-6
+    for which, mine in ((0, dq), (1, dk), (2, dv)):
+        base = (q, k, v)[which]
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(*base.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += h
+            lp = _loss_gqa(*args, do, opts)
+            args[which][idx] -= 2 * h
+            lm = _loss_gqa(*args, do, opts)
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.linalg.norm(mine - fd) / max(np.linalg.norm(fd), 1e-30) < 1e-6
+
+
+def test_gqa_with_one_group_is_per_head_attention():
+    # H_kv = H: the grouped form reduces to independent heads.
+    r = rng(11)
+    q, k, v, do = (r.standard_normal((2, 3, 9, 4)) for _ in range(4))
+    o1, l1 = oracle.fwd_gqa(q, k, v, 0.5, causal=True)
+    o2, l2 = oracle.fwd(q, k, v, 0.5, causal=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_mqa_heads_share_keys():
+    # H_kv = 1: two query heads with equal queries see the same K/V, so their
+    # outputs are equal; with different queries they generally differ.
+    r = rng(12)
+    q1 = r.standard_normal((1, 1, 7, 4))
+    q = np.concatenate([q1, q1, r.standard_normal((1, 1, 7, 4))], axis=1)
+    k, v = r.standard_normal((2, 1, 1, 7, 4))
+    o, _ = oracle.fwd_gqa(q, k, v, 0.5)
+    assert np.max(np.abs(o[0, 0] - o[0, 1])) < 1e-15
+    assert np.max(np.abs(o[0, 0] - o[0, 2])) > 1e-3
