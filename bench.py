@@ -39,7 +39,7 @@ DEFAULT_WORKLOAD = "gpt2_medium"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 # algorithmic flops per allowed pair for each tensor-core kernel (per unit of d)
-KERNEL_FLOPS_PER_PAIR_D = {"fwd": 4, "bwd_dkdv": 8, "bwd_dq": 6}
+KERNEL_FLOPS_PER_PAIR_D = {"fwd": 4, "bwd_dkdv": 8, "bwd_dq": 6, "bwd": 10}
 
 
 # --------------------------------------------------------------------- work model
@@ -180,9 +180,14 @@ class Step:
         if w.butterfly:
             self.bm = fa.fa_butterfly_mask(math.ceil(w.N / 128)).to(dev)
         B, H, N, d = w.B, w.H, w.N, w.d
+        # grouped K/V heads go through fa_fwd_gqa / fa_bwd_gqa, timed as fwd and
+        # the whole backward (the per-stage entry points are per-head only)
+        self.gqa = w.kv_heads != H
+        self.kernels = ("fwd", "bwd") if self.gqa else KERNELS
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.dq = torch.empty_like(self.q)
+        self.dk, self.dv = torch.empty_like(self.k), torch.empty_like(self.v)
         self.ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.opts = dict(causal=w.causal, dropout_p=w.dropout_p, seed=0, offset=0,
@@ -193,6 +198,21 @@ class Step:
         B, H, N, d, s = w.B, w.H, w.N, w.d, w.scale
         o = self.opts
         ev = events or [None] * 5
+        if self.gqa:
+            Hkv = w.kv_heads
+            if ev[0] is not None:
+                ev[0].record()
+            st = fa.fa_fwd_gqa(self.q, self.k, self.v, self.o, self.lse, B, H, Hkv, N, d, s, **o)
+            if ev[1] is not None:
+                ev[1].record()
+            st |= fa.fa_bwd_gqa(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq,
+                                self.dk, self.dv, B, H, Hkv, N, d, s, workspace=self.ws,
+                                workspace_bytes=self.ws_bytes, **o)
+            if ev[2] is not None:
+                ev[2].record()
+            if st != 0:
+                raise RuntimeError(f"library call failed with status {st}")
+            return
         if ev[0] is not None:
             ev[0].record()
         st = fa.fa_fwd(self.q, self.k, self.v, self.o, self.lse, B, H, N, d, s, **o)
@@ -252,6 +272,7 @@ def cpu_baseline(w, x, seqlens, budget_s=15.0):
     """Time the fp64 oracle (fwd + bwd) on a bounded sample of heads."""
     import oracle
     heads_all = [(b, h) for b in range(w.B) for h in range(w.H)]
+    G = w.H // w.kv_heads  # query heads per K/V head
     sl_np = None if seqlens is None else seqlens.numpy()
     bm = None
     if w.butterfly:
@@ -259,7 +280,9 @@ def cpu_baseline(w, x, seqlens, budget_s=15.0):
 
     def run(heads):
         f64 = lambda t: np.stack([t[b, h].double().numpy() for b, h in heads])
-        q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
+        f64kv = lambda t: np.stack([t[b, h // G].double().numpy() for b, h in heads])
+        q, do = f64(x["q"]), f64(x["do"])
+        k, v = f64kv(x["k"]), f64kv(x["v"])
         t0 = time.perf_counter()
         kw = dict(causal=w.causal, dropout_p=w.dropout_p, seed=0, offset=0, block_mask=bm,
                   seqlens_k=sl_np, heads=heads, H=w.H)
@@ -346,9 +369,9 @@ def run_ours(args, w):
     barrier(pg)
     elapsed = start.elapsed_time(end) / 1e3
     elapsed = max_over_ranks(pg, elapsed)
-    per_kernel = {k: [] for k in KERNELS}
+    per_kernel = {k: [] for k in step.kernels}
     for e in evs:
-        for j, k in enumerate(KERNELS):
+        for j, k in enumerate(step.kernels):
             per_kernel[k].append(e[j].elapsed_time(e[j + 1]) / 1e3)
     kstats = {k: statistics.mean(v) for k, v in per_kernel.items()}
     assert step.fa.fa_device_status() == 0, "device-side error during the timed region"
@@ -399,6 +422,7 @@ def run_ours(args, w):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; no dataset)",
         "config": {"workload": w.name, "description": w.description, "B": w.B, "H": w.H,
+                   "H_kv": w.kv_heads,
                    "N": w.N, "d": w.d, "causal": w.causal, "dropout_p": w.dropout_p,
                    "key_padding": w.padding, "block_mask": "butterfly" if w.butterfly else None,
                    "allowed_pairs": pairs, "flops_per_step": flops_step,
@@ -443,7 +467,7 @@ def run_reference(args, w):
     bm = oracle.butterfly(math.ceil(w.N / 128)) if w.butterfly else None
     heads = [(0, 0)]
     f64 = lambda t: np.stack([t[b, h].double().numpy() for b, h in heads])
-    q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
+    q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))  # head 0 uses K/V head 0
     kw = dict(causal=w.causal, dropout_p=w.dropout_p, seed=0, offset=0, block_mask=bm,
               seqlens_k=sl_np, heads=heads, H=w.H)
     wb = inputs.Workload("s", 1, 1, w.N, w.d, causal=w.causal, butterfly=w.butterfly)

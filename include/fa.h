@@ -90,6 +90,29 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
                  size_t workspace_bytes, void* stream);
 
+/* Grouped-query attention (query heads sharing K/V heads, which the page
+ * "Attention Kernel: FlashAttention 与它的后继者", section on FlashAttention's
+ * IO-aware insight, names as a further cut of K/V reads): H query heads and
+ * H_kv K/V heads, H a multiple of H_kv, query head h of batch row b attending
+ * with K/V head h / (H / H_kv).
+ * q, o, dout, dq: bf16 [B,H,N,d]; k, v, dk, dv: bf16 [B,H_kv,N,d]; lse:
+ * fp32 [B,H,N]. dk and dv of a K/V head are the sums over the query heads
+ * that share it, formed on chip (the key-tile kernel walks every query head
+ * of the group), so they stay atomic-free and deterministic. Dropout keys on
+ * the query head, as for H independent heads. H_kv = H is fa_fwd / fa_bwd;
+ * H_kv = 1 is multi-query attention. Errors as for fa_fwd / fa_bwd, plus
+ * FA_ERR_INVALID_ARG when H_kv < 1 or H % H_kv != 0. The workspace is
+ * fa_bwd_workspace_size(B, H, N, d). */
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int H_kv, int N, int d, float scale, int causal, float dropout_p,
+                     uint64_t seed, uint64_t offset, const uint8_t* block_mask,
+                     const int32_t* seqlens_k, void* stream);
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N,
+                     int d, float scale, int causal, float dropout_p, uint64_t seed,
+                     uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* The three stages fa_bwd runs, for callers that schedule or time them
  * separately. They must run in this order on one stream with the same
  * workspace (it carries D from the first stage to the other two); dK/dV and

@@ -31,7 +31,8 @@ FA_ERR_TIMEOUT = 5
 
 # Symbols declared in include/fa.h.
 EXPORTS = (
-    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq",
+    "fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_workspace_size", "fa_bwd_preprocess",
+    "fa_bwd_dkdv", "fa_bwd_dq",
     "fa_bwd_noalloc", "fa_dropout_p8", "fa_debug_dropout_keep",
     "fa_debug_philox", "fa_butterfly_mask", "fa_device_status", "fa_set_wait_timeout_ns",
     "fa_test_inject_stall", "fa_status_string",
@@ -70,6 +71,12 @@ def load(build_if_missing: bool = False):
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u64,
                                vp, vp, vp, sz, vp]
         lib.fa_bwd.restype = i
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, u64, u64, vp, vp,
+                                   vp]
+        lib.fa_fwd_gqa.restype = i
+        lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, u64,
+                                   u64, vp, vp, vp, sz, vp]
+        lib.fa_bwd_gqa.restype = i
         lib.fa_bwd_preprocess.argtypes = [vp, vp, i, i, i, i, vp, sz, vp]
         lib.fa_bwd_preprocess.restype = i
         lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u64, vp,
@@ -132,6 +139,15 @@ def _check_qkv(*ts):
             raise ValueError("expected contiguous 4-D bf16 CUDA tensors [B, H, N, d]")
 
 
+def _kv_heads(q, k, v) -> int:
+    """K/V head count; q [B, H, N, d] with k, v [B, H_kv, N, d], H a multiple of H_kv."""
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, N, d) or tuple(v.shape) != tuple(k.shape) or H % Hkv != 0:
+        raise ValueError("k and v must be [B, H_kv, N, d] with H a multiple of H_kv")
+    return Hkv
+
+
 def _opt_ptrs(block_mask, seqlens_k):
     if block_mask is not None and (block_mask.dtype != torch.uint8 or not block_mask.is_cuda
                                    or not block_mask.is_contiguous()):
@@ -163,6 +179,24 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal=False, d
                          _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                          float(dropout_p), int(seed), int(offset), bm, sl, _ptr(workspace),
                          int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal=False, dropout_p=0.0, seed=0,
+               offset=0, block_mask=None, seqlens_k=None, stream=None) -> int:
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N, d,
+                             float(scale), int(bool(causal)), float(dropout_p), int(seed),
+                             int(offset), bm, sl, _stream(stream))
+
+
+def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal=False,
+               dropout_p=0.0, seed=0, offset=0, block_mask=None, seqlens_k=None, workspace=None,
+               workspace_bytes=0, stream=None) -> int:
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, H, H_kv, N, d, float(scale),
+                             int(bool(causal)), float(dropout_p), int(seed), int(offset), bm, sl,
+                             _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_bwd_preprocess(o, dout, B, H, N, d, workspace, workspace_bytes, stream=None) -> int:
@@ -239,29 +273,44 @@ def fa_test_inject_stall(mode: int) -> None:
 
 def fwd(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0, block_mask=None,
         seqlens_k=None, stream=None):
-    """Allocate O and lse with torch and run fa_fwd. Returns (o, lse)."""
+    """Allocate O and lse with torch and run fa_fwd (fa_fwd_gqa when k and v
+    have fewer heads than q). Returns (o, lse)."""
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
+    Hkv = _kv_heads(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _check(fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dropout_p, seed, offset, block_mask,
-                  seqlens_k, stream), "fa_fwd")
+    if Hkv == H:
+        st = fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dropout_p, seed, offset,
+                    block_mask, seqlens_k, stream)
+    else:
+        st = fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, dropout_p, seed, offset,
+                        block_mask, seqlens_k, stream)
+    _check(st, "fa_fwd")
     return o, lse
 
 
 def bwd(q, k, v, o, dout, lse, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0,
         block_mask=None, seqlens_k=None, workspace=None, stream=None):
-    """Allocate dQ, dK, dV (and the workspace if not given) and run fa_bwd."""
+    """Allocate dQ, dK, dV (and the workspace if not given) and run fa_bwd
+    (fa_bwd_gqa when k and v have fewer heads than q)."""
     _check_qkv(q, k, v, o, dout)
     B, H, N, d = q.shape
+    Hkv = _kv_heads(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws_bytes = fa_bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    _check(fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dropout_p, seed,
-                  offset, block_mask, seqlens_k, workspace, workspace.numel(), stream), "fa_bwd")
+    if Hkv == H:
+        st = fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dropout_p, seed,
+                    offset, block_mask, seqlens_k, workspace, workspace.numel(), stream)
+    else:
+        st = fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal,
+                        dropout_p, seed, offset, block_mask, seqlens_k, workspace,
+                        workspace.numel(), stream)
+    _check(st, "fa_bwd")
     return dq, dk, dv

@@ -80,8 +80,9 @@ int p8_of(float p) {
   return v >= 256 ? -1 : v;
 }
 
-fa_status check_common(int B, int H, int N, int d, float scale, float dropout_p) {
+fa_status check_common(int B, int H, int N, int d, float scale, float dropout_p, int Hkv) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(B) * H * N;
   if (rows >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -107,10 +108,12 @@ bool encode_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-fa::MaskParams make_mask(int B, int H, int N, int causal, const uint8_t* bm, const int32_t* sl) {
+fa::MaskParams make_mask(int B, int H, int Hkv, int N, int causal, const uint8_t* bm,
+                         const int32_t* sl) {
   fa::MaskParams m;
   m.B = B;
   m.H = H;
+  m.Hkv = Hkv;
   m.N = N;
   m.nb = (N + fa::kTile - 1) / fa::kTile;
   m.causal = causal ? 1 : 0;
@@ -160,11 +163,11 @@ std::mutex g_noalloc_mutex;
 
 extern "C" {
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                 int N, int d, float scale, int causal, float dropout_p, uint64_t seed,
-                 uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
-                 void* stream) {
-  fa_status st = check_common(B, H, N, d, scale, dropout_p);
+static fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int H, int Hkv, int N, int d, float scale, int causal, float dropout_p,
+                          uint64_t seed, uint64_t offset, const uint8_t* block_mask,
+                          const int32_t* seqlens_k, void* stream) {
+  fa_status st = check_common(B, H, N, d, scale, dropout_p, Hkv);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
@@ -172,11 +175,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
   CUtensorMap tq, tk, tv;
-  if (!encode_map(&tq, q, B * H, N, d) || !encode_map(&tk, k, B * H, N, d) ||
-      !encode_map(&tv, v, B * H, N, d))
+  if (!encode_map(&tq, q, B * H, N, d) || !encode_map(&tk, k, B * Hkv, N, d) ||
+      !encode_map(&tv, v, B * Hkv, N, d))
     return FA_ERR_CUDA;
   fa::FwdArgs a;
-  a.mask = make_mask(B, H, N, causal, block_mask, seqlens_k);
+  a.mask = make_mask(B, H, Hkv, N, causal, block_mask, seqlens_k);
   a.drop = make_drop(dropout_p, seed, offset);
   a.sync = make_sync(di, true);
   a.scale_log2 = scale * fa::kLog2e;
@@ -185,6 +188,22 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   cudaError_t e = fa::launch_fwd(tq, tk, tv, a, d, a.drop.p8 > 0, di->num_sms,
                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, float dropout_p, uint64_t seed,
+                 uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
+                 void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, H, N, d, scale, causal, dropout_p, seed, offset,
+                  block_mask, seqlens_k, stream);
+}
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int H_kv, int N, int d, float scale, int causal, float dropout_p,
+                     uint64_t seed, uint64_t offset, const uint8_t* block_mask,
+                     const int32_t* seqlens_k, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, dropout_p, seed, offset,
+                  block_mask, seqlens_k, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -197,11 +216,12 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 // pointers must be present: 1 = preprocess (o, dout), 2 = dK/dV, 4 = dQ.
 static fa_status bwd_prepare(const void* q, const void* k, const void* v, const void* o,
                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                             int B, int H, int N, int d, float scale, int causal, float dropout_p,
-                             uint64_t seed, uint64_t offset, const uint8_t* block_mask,
-                             const int32_t* seqlens_k, void* workspace, size_t workspace_bytes,
-                             int need, fa::BwdArgs* a, CUtensorMap* maps, DeviceInfo** di) {
-  fa_status st = check_common(B, H, N, d, scale, dropout_p);
+                             int B, int H, int Hkv, int N, int d, float scale, int causal,
+                             float dropout_p, uint64_t seed, uint64_t offset,
+                             const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                             size_t workspace_bytes, int need, fa::BwdArgs* a, CUtensorMap* maps,
+                             DeviceInfo** di) {
+  fa_status st = check_common(B, H, N, d, scale, dropout_p, Hkv);
   if (st != FA_OK) return st;
   if (need & 1) {
     if (!o || !dout || !aligned16(o) || !aligned16(dout)) return FA_ERR_INVALID_ARG;
@@ -219,11 +239,11 @@ static fa_status bwd_prepare(const void* q, const void* k, const void* v, const 
     return FA_ERR_WORKSPACE;
   if ((st = device_info(di)) != FA_OK) return st;
   if (need & 6) {
-    if (!encode_map(&maps[0], q, B * H, N, d) || !encode_map(&maps[1], k, B * H, N, d) ||
-        !encode_map(&maps[2], v, B * H, N, d) || !encode_map(&maps[3], dout, B * H, N, d))
+    if (!encode_map(&maps[0], q, B * H, N, d) || !encode_map(&maps[1], k, B * Hkv, N, d) ||
+        !encode_map(&maps[2], v, B * Hkv, N, d) || !encode_map(&maps[3], dout, B * H, N, d))
       return FA_ERR_CUDA;
   }
-  a->mask = make_mask(B, H, N, causal, block_mask, seqlens_k);
+  a->mask = make_mask(B, H, Hkv, N, causal, block_mask, seqlens_k);
   a->drop = make_drop(dropout_p, seed, offset);
   a->sync = make_sync(*di, false);
   a->scale = scale;
@@ -238,15 +258,16 @@ static fa_status bwd_prepare(const void* q, const void* k, const void* v, const 
   return FA_OK;
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                 float scale, int causal, float dropout_p, uint64_t seed, uint64_t offset,
-                 const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                          int H, int Hkv, int N, int d, float scale, int causal, float dropout_p,
+                          uint64_t seed, uint64_t offset, const uint8_t* block_mask,
+                          const int32_t* seqlens_k, void* workspace, size_t workspace_bytes,
+                          void* stream) {
   fa::BwdArgs a;
   CUtensorMap m[4];
   DeviceInfo* di = nullptr;
-  fa_status st = bwd_prepare(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal,
+  fa_status st = bwd_prepare(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal,
                              dropout_p, seed, offset, block_mask, seqlens_k, workspace,
                              workspace_bytes, 7, &a, m, &di);
   if (st != FA_OK) return st;
@@ -258,13 +279,31 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, float dropout_p, uint64_t seed, uint64_t offset,
+                 const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, N, d, scale, causal, dropout_p, seed,
+                  offset, block_mask, seqlens_k, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N,
+                     int d, float scale, int causal, float dropout_p, uint64_t seed,
+                     uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal, dropout_p,
+                  seed, offset, block_mask, seqlens_k, workspace, workspace_bytes, stream);
+}
+
 fa_status fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int N, int d,
                             void* workspace, size_t workspace_bytes, void* stream) {
   fa::BwdArgs a;
   CUtensorMap m[4];
   DeviceInfo* di = nullptr;
   fa_status st = bwd_prepare(nullptr, nullptr, nullptr, o, dout, nullptr, nullptr, nullptr,
-                             nullptr, B, H, N, d, 1.f, 0, 0.f, 0, 0, nullptr, nullptr, workspace,
+                             nullptr, B, H, H, N, d, 1.f, 0, 0.f, 0, 0, nullptr, nullptr, workspace,
                              workspace_bytes, 1, &a, m, &di);
   if (st != FA_OK) return st;
   return fa::launch_bwd_preprocess(a, d, di->num_sms, static_cast<cudaStream_t>(stream)) ==
@@ -281,7 +320,7 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
   fa::BwdArgs a;
   CUtensorMap m[4];
   DeviceInfo* di = nullptr;
-  fa_status st = bwd_prepare(q, k, v, nullptr, dout, lse, nullptr, dk, dv, B, H, N, d, scale,
+  fa_status st = bwd_prepare(q, k, v, nullptr, dout, lse, nullptr, dk, dv, B, H, H, N, d, scale,
                              causal, dropout_p, seed, offset, block_mask, seqlens_k, workspace,
                              workspace_bytes, 2, &a, m, &di);
   if (st != FA_OK) return st;
@@ -299,7 +338,7 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dou
   fa::BwdArgs a;
   CUtensorMap m[4];
   DeviceInfo* di = nullptr;
-  fa_status st = bwd_prepare(q, k, v, nullptr, dout, lse, dq, nullptr, nullptr, B, H, N, d,
+  fa_status st = bwd_prepare(q, k, v, nullptr, dout, lse, dq, nullptr, nullptr, B, H, H, N, d,
                              scale, causal, dropout_p, seed, offset, block_mask, seqlens_k,
                              workspace, workspace_bytes, 4, &a, m, &di);
   if (st != FA_OK) return st;

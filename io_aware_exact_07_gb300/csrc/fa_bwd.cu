@@ -104,7 +104,7 @@ struct DkdvLayout {
   __device__ static constexpr uint32_t col_dpt() { return static_cast<uint32_t>(2 * D + 128); }
 };
 
-template <int D, bool DROPOUT>
+template <int D, bool DROPOUT, bool GQA>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -119,9 +119,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int lane = tid & 31;
   const MaskParams& mk = args.mask;
   const int N = mk.N;
-  const int BH = mk.B * mk.H;
   const int n_t = (N + kTile - 1) / kTile;  // query tiles == key tiles
-  const int n_units = BH * n_t;
+  const int n_units = mk.B * mk.Hkv * n_t;
+  const int G = GQA ? mk.H / mk.Hkv : 1;  // query heads per K/V head
 
   uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bh = u / n_t, kt = u % n_t;
-      const int b = bh / mk.H;
+      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+      const int b = bhk / mk.Hkv;
       const int kv_len = kv_len_of(mk, b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       if (unit_count > 0 && !mbar_wait_warp(b_kv_empty, (unit_count - 1) & 1, tmo, abort_flag)) {
@@ -199,51 +199,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) {
         mbar_expect_tx(b_kv_full, 2 * L::kTileBytes);
         for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_3d(sK + c * 16384, &tm_k, c * 64, kt * kTile, bh, b_kv_full);
-          tma_load_3d(sV + c * 16384, &tm_v, c * 64, kt * kTile, bh, b_kv_full);
+          tma_load_3d(sK + c * 16384, &tm_k, c * 64, kt * kTile, bhk, b_kv_full);
+          tma_load_3d(sV + c * 16384, &tm_v, c * 64, kt * kTile, bhk, b_kv_full);
         }
       }
       ++kv_arms;
-      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
-        while (bits != 0u) {
-          const int qt = chunk * 32 + (__ffs(bits) - 1);
-          bits &= bits - 1;
-          const int s = it % L::kStages;
-          const uint32_t ph = (it / L::kStages) & 1u;
-          if (!mbar_wait_warp(b_q_empty[s], ph ^ 1u, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          // lse (log2 units) and D of the 128 query rows of this tile
-          float4 l4, d4;
-          float* lp = &l4.x;
-          float* dp = &d4.x;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int row = qt * kTile + 4 * lane + r;
-            const bool in = row < N;
-            const long long idx = static_cast<long long>(bh) * N + row;
-            lp[r] = -lse2_of(args.lse, idx, in);
-            dp[r] = in ? -args.dsum[idx] : 0.f;
-          }
-          // staged negated: the compute warps add them as packed pairs
-          reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
-          reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
-          if (lane == 0) {
-            mbar_expect_tx(b_q_full[s], 2 * L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c) {
-              tma_load_3d(sQ + s * L::kTileBytes + c * 16384, &tm_q, c * 64, qt * kTile, bh,
-                          b_q_full[s]);
-              tma_load_3d(sDO + s * L::kTileBytes + c * 16384, &tm_do, c * 64, qt * kTile, bh,
-                          b_q_full[s]);
+      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+             ++bh) {  // the query heads sharing this K/V head
+        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          while (bits != 0u) {
+            const int qt = chunk * 32 + (__ffs(bits) - 1);
+            bits &= bits - 1;
+            const int s = it % L::kStages;
+            const uint32_t ph = (it / L::kStages) & 1u;
+            if (!mbar_wait_warp(b_q_empty[s], ph ^ 1u, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
             }
-          } else {
-            mbar_arrive(b_q_full[s]);
+            // lse (log2 units) and D of the 128 query rows of this tile
+            float4 l4, d4;
+            float* lp = &l4.x;
+            float* dp = &d4.x;
+  #pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int row = qt * kTile + 4 * lane + r;
+              const bool in = row < N;
+              const long long idx = static_cast<long long>(bh) * N + row;
+              lp[r] = -lse2_of(args.lse, idx, in);
+              dp[r] = in ? -args.dsum[idx] : 0.f;
+            }
+            // staged negated: the compute warps add them as packed pairs
+            reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
+            reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
+            if (lane == 0) {
+              mbar_expect_tx(b_q_full[s], 2 * L::kTileBytes);
+              for (int c = 0; c < L::kChunks; ++c) {
+                tma_load_3d(sQ + s * L::kTileBytes + c * 16384, &tm_q, c * 64, qt * kTile, bh,
+                            b_q_full[s]);
+                tma_load_3d(sDO + s * L::kTileBytes + c * 16384, &tm_do, c * 64, qt * kTile, bh,
+                            b_q_full[s]);
+              }
+            } else {
+              mbar_arrive(b_q_full[s]);
+            }
+            ++q_arms;
+            ++it;
           }
-          ++q_arms;
-          ++it;
         }
       }
     }
@@ -280,11 +283,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     };
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bh = u / n_t, kt = u % n_t;
-      const int b = bh / mk.H;
+      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+      const int b = bhk / mk.Hkv;
       const int kv_len = kv_len_of(mk, b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
-      (void)bh;
       if (!mbar_wait_warp(b_kv_full, unit_count & 1, tmo, abort_flag)) {
         fail();
         ok = false;
@@ -292,60 +294,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       int t = 0;
       int prev_s = -1;
-      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
-        while (bits != 0u) {
-          bits &= bits - 1;
-          const int s = it % L::kStages;
-          const uint32_t ph = (it / L::kStages) & 1u;
-          if (!mbar_wait_warp(b_q_full[s], ph, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (elected) {
-            issue_ss(L::col_st(), sK, sQ + s * L::kTileBytes);  // S^T = K Q^T
-            mma_commit(b_st_full);
-          }
-          __syncwarp();
-          if (t > 0) {  // dK += dS^T(prev) Q(prev)
-            if (!mbar_wait_warp(b_ds_ready, ds_cnt & 1, tmo, abort_flag)) {
+      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+             ++bh) {  // the query heads sharing this K/V head
+        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          while (bits != 0u) {
+            bits &= bits - 1;
+            const int s = it % L::kStages;
+            const uint32_t ph = (it / L::kStages) & 1u;
+            if (!mbar_wait_warp(b_q_full[s], ph, tmo, abort_flag)) {
               fail();
               ok = false;
               break;
             }
-            ++ds_cnt;
             tc_fence_after();
             if (elected) {
-              issue_acc(L::col_dk(), L::col_dpt(), sQ + prev_s * L::kTileBytes, t - 1 > 0);
-              mma_commit(b_q_empty[prev_s]);
+              issue_ss(L::col_st(), sK, sQ + s * L::kTileBytes);  // S^T = K Q^T
+              mma_commit(b_st_full);
             }
             __syncwarp();
+            if (t > 0) {  // dK += dS^T(prev) Q(prev)
+              if (!mbar_wait_warp(b_ds_ready, ds_cnt & 1, tmo, abort_flag)) {
+                fail();
+                ok = false;
+                break;
+              }
+              ++ds_cnt;
+              tc_fence_after();
+              if (elected) {
+                issue_acc(L::col_dk(), L::col_dpt(), sQ + prev_s * L::kTileBytes, t - 1 > 0);
+                mma_commit(b_q_empty[prev_s]);
+              }
+              __syncwarp();
+            }
+            if (elected) {
+              issue_ss(L::col_dpt(), sV, sDO + s * L::kTileBytes);  // dP^T = V dO^T
+              mma_commit(b_dpt_full);
+            }
+            __syncwarp();
+            if (!mbar_wait_warp(b_p_ready, p_cnt & 1, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            ++p_cnt;
+            if (t == 0 && unit_count > 0 &&
+                !mbar_wait_warp(b_acc_free, (unit_count - 1) & 1, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elected) issue_acc(L::col_dv(), L::col_st(), sDO + s * L::kTileBytes, t > 0);
+            __syncwarp();
+            prev_s = s;
+            ++t;
+            ++it;
           }
-          if (elected) {
-            issue_ss(L::col_dpt(), sV, sDO + s * L::kTileBytes);  // dP^T = V dO^T
-            mma_commit(b_dpt_full);
-          }
-          __syncwarp();
-          if (!mbar_wait_warp(b_p_ready, p_cnt & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          ++p_cnt;
-          if (t == 0 && unit_count > 0 &&
-              !mbar_wait_warp(b_acc_free, (unit_count - 1) & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (elected) issue_acc(L::col_dv(), L::col_st(), sDO + s * L::kTileBytes, t > 0);
-          __syncwarp();
-          prev_s = s;
-          ++t;
-          ++it;
         }
       }
       if (!ok) break;
@@ -392,148 +397,151 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bh = u / n_t, kt = u % n_t;
-      const int b = bh / mk.H;
+      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+      const int b = bhk / mk.Hkv;
       const int kv_len = kv_len_of(mk, b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int key = kt * kTile + r;
       int n_done = 0;
-      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
-        while (bits != 0u) {
-          const int qt = chunk * 32 + (__ffs(bits) - 1);
-          bits &= bits - 1;
-          const int s = it % L::kStages;
-          const float* lse_t = lse_s + s * 128 + 64 * wg;
-          const float* dsum_t = dsum_s + s * 128 + 64 * wg;
-          const int q0 = qt * kTile + 64 * wg;  // first query column of this thread's half
-          // Dropout keep bits of this (key, 64 queries) strip.
-          uint32_t zb0 = 0xFFFFFFFFu, zb1 = 0xFFFFFFFFu;
-          if constexpr (DROPOUT) {
-            const uint32_t key0 = static_cast<uint32_t>(kt * kTile + quad * 32);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int idx = lane + 32 * m;
-              const int c = idx >> 1, gs = idx & 1;
-              const uint32_t rowg = static_cast<uint32_t>(bh) * static_cast<uint32_t>(N) +
-                                    static_cast<uint32_t>(q0 + c);
-              const uint4 kw = dropout_keep16(args.drop, rowg, (key0 >> 4) + gs);
-              reinterpret_cast<uint4*>(drop_scratch)[c * 2 + gs] = kw;
-            }
-            __syncwarp();
-            zb0 = 0u;
-            zb1 = 0u;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const uint32_t w = drop_scratch[(c * 2 + (lane >> 4)) * 4 + ((lane & 15) >> 2)];
-              const uint32_t kbit = (w >> (8 * (lane & 3))) & 1u;  // bytes are 0x00 or 0xFF
-              if (c < 32) zb0 |= kbit << c;
-              else zb1 |= kbit << (c - 32);
-            }
-            __syncwarp();
-          }
-          // ---- phase 1: P^T
-          if (!mbar_wait_warp(b_st_full, st_cnt & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          ++st_cnt;
-          tc_fence_after();
-          float p[64];
-          {
-            uint32_t sr[64];
-            tmem_ld32(tSt, &sr[0]);
-            tmem_ld32(tSt + 32, &sr[32]);
-            tmem_ld_wait();
-            const uint64_t c2 = f2_pack(c_log2, c_log2);
-#pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4) {
-              const ulonglong2 nl = reinterpret_cast<const ulonglong2*>(lse_t)[c4];  // -lse2 pairs
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int c = 4 * c4 + 2 * h;
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2,
-                                 h ? nl.y : nl.x),
-                          x0, x1);
-                p[c] = ex2_approx(x0);
-                p[c + 1] = ex2_approx(x1);
+      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+             ++bh) {  // the query heads sharing this K/V head
+        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          while (bits != 0u) {
+            const int qt = chunk * 32 + (__ffs(bits) - 1);
+            bits &= bits - 1;
+            const int s = it % L::kStages;
+            const float* lse_t = lse_s + s * 128 + 64 * wg;
+            const float* dsum_t = dsum_s + s * 128 + 64 * wg;
+            const int q0 = qt * kTile + 64 * wg;  // first query column of this thread's half
+            // Dropout keep bits of this (key, 64 queries) strip.
+            uint32_t zb0 = 0xFFFFFFFFu, zb1 = 0xFFFFFFFFu;
+            if constexpr (DROPOUT) {
+              const uint32_t key0 = static_cast<uint32_t>(kt * kTile + quad * 32);
+  #pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int idx = lane + 32 * m;
+                const int c = idx >> 1, gs = idx & 1;
+                const uint32_t rowg = static_cast<uint32_t>(bh) * static_cast<uint32_t>(N) +
+                                      static_cast<uint32_t>(q0 + c);
+                const uint4 kw = dropout_keep16(args.drop, rowg, (key0 >> 4) + gs);
+                reinterpret_cast<uint4*>(drop_scratch)[c * 2 + gs] = kw;
               }
-            }
-          }
-          if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
-            const bool key_ok = key < kv_len;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const bool allowed = key_ok && (!mk.causal || key <= q0 + c);
-              p[c] = allowed ? p[c] : 0.f;
-            }
-          }
-          {
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              float a0 = p[2 * c], a1 = p[2 * c + 1];
-              if constexpr (DROPOUT) {
-                const uint32_t zw = (c < 16) ? zb0 : zb1;
-                const int sh = (2 * c) & 31;
-                a0 = ((zw >> sh) & 1u) ? a0 : 0.f;
-                a1 = ((zw >> (sh + 1)) & 1u) ? a1 : 0.f;
+              __syncwarp();
+              zb0 = 0u;
+              zb1 = 0u;
+  #pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const uint32_t w = drop_scratch[(c * 2 + (lane >> 4)) * 4 + ((lane & 15) >> 2)];
+                const uint32_t kbit = (w >> (8 * (lane & 3))) & 1u;  // bytes are 0x00 or 0xFF
+                if (c < 32) zb0 |= kbit << c;
+                else zb1 |= kbit << (c - 32);
               }
-              pk[c] = pack_bf16x2(a0, a1);
+              __syncwarp();
             }
-            tmem_st32(tSt, pk);
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(b_p_ready);
-          // ---- phase 2: dS^T
-          if (!mbar_wait_warp(b_dpt_full, dpt_cnt & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          ++dpt_cnt;
-          tc_fence_after();
-          {
-            uint32_t pk[32];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t dr[32];
-              tmem_ld32(tDPt + 32 * h, dr);
+            // ---- phase 1: P^T
+            if (!mbar_wait_warp(b_st_full, st_cnt & 1, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            ++st_cnt;
+            tc_fence_after();
+            float p[64];
+            {
+              uint32_t sr[64];
+              tmem_ld32(tSt, &sr[0]);
+              tmem_ld32(tSt + 32, &sr[32]);
               tmem_ld_wait();
-#pragma unroll
-              for (int c4 = 0; c4 < 8; ++c4) {
-                const ulonglong2 nd = reinterpret_cast<const ulonglong2*>(dsum_t)[8 * h + c4];  // -D
-#pragma unroll
-                for (int e = 0; e < 4; e += 2) {
-                  const int c = 32 * h + 4 * c4 + e;
-                  float z0 = args.drop.keep_scale, z1 = args.drop.keep_scale;
-                  if constexpr (DROPOUT) {
-                    const uint32_t zw = (c < 32) ? zb0 : zb1;
-                    z0 = ((zw >> (c & 31)) & 1u) ? z0 : 0.f;
-                    z1 = ((zw >> ((c + 1) & 31)) & 1u) ? z1 : 0.f;
-                  }
-                  const uint64_t t = f2_fma(f2_pack(z0, z1),
-                                            f2_pack(__uint_as_float(dr[4 * c4 + e]),
-                                                    __uint_as_float(dr[4 * c4 + e + 1])),
-                                            e ? nd.y : nd.x);
-                  float a0, a1;
-                  f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), a0, a1);
-                  pk[16 * h + 2 * c4 + (e >> 1)] = pack_bf16x2(a0, a1);
+              const uint64_t c2 = f2_pack(c_log2, c_log2);
+  #pragma unroll
+              for (int c4 = 0; c4 < 16; ++c4) {
+                const ulonglong2 nl = reinterpret_cast<const ulonglong2*>(lse_t)[c4];  // -lse2 pairs
+  #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int c = 4 * c4 + 2 * h;
+                  float x0, x1;
+                  f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2,
+                                   h ? nl.y : nl.x),
+                            x0, x1);
+                  p[c] = ex2_approx(x0);
+                  p[c + 1] = ex2_approx(x1);
                 }
               }
             }
-            tmem_st32(tDPt, pk);
+            if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
+              const bool key_ok = key < kv_len;
+  #pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const bool allowed = key_ok && (!mk.causal || key <= q0 + c);
+                p[c] = allowed ? p[c] : 0.f;
+              }
+            }
+            {
+              uint32_t pk[32];
+  #pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                float a0 = p[2 * c], a1 = p[2 * c + 1];
+                if constexpr (DROPOUT) {
+                  const uint32_t zw = (c < 16) ? zb0 : zb1;
+                  const int sh = (2 * c) & 31;
+                  a0 = ((zw >> sh) & 1u) ? a0 : 0.f;
+                  a1 = ((zw >> (sh + 1)) & 1u) ? a1 : 0.f;
+                }
+                pk[c] = pack_bf16x2(a0, a1);
+              }
+              tmem_st32(tSt, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(b_p_ready);
+            // ---- phase 2: dS^T
+            if (!mbar_wait_warp(b_dpt_full, dpt_cnt & 1, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            ++dpt_cnt;
+            tc_fence_after();
+            {
+              uint32_t pk[32];
+  #pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t dr[32];
+                tmem_ld32(tDPt + 32 * h, dr);
+                tmem_ld_wait();
+  #pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                  const ulonglong2 nd = reinterpret_cast<const ulonglong2*>(dsum_t)[8 * h + c4];  // -D
+  #pragma unroll
+                  for (int e = 0; e < 4; e += 2) {
+                    const int c = 32 * h + 4 * c4 + e;
+                    float z0 = args.drop.keep_scale, z1 = args.drop.keep_scale;
+                    if constexpr (DROPOUT) {
+                      const uint32_t zw = (c < 32) ? zb0 : zb1;
+                      z0 = ((zw >> (c & 31)) & 1u) ? z0 : 0.f;
+                      z1 = ((zw >> ((c + 1) & 31)) & 1u) ? z1 : 0.f;
+                    }
+                    const uint64_t t = f2_fma(f2_pack(z0, z1),
+                                              f2_pack(__uint_as_float(dr[4 * c4 + e]),
+                                                      __uint_as_float(dr[4 * c4 + e + 1])),
+                                              e ? nd.y : nd.x);
+                    float a0, a1;
+                    f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), a0, a1);
+                    pk[16 * h + 2 * c4 + (e >> 1)] = pack_bf16x2(a0, a1);
+                  }
+                }
+              }
+              tmem_st32(tDPt, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(b_ds_ready);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_q_empty[s]);  // lse / D of this stage no longer read
+            ++n_done;
+            ++it;
           }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(b_ds_ready);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(b_q_empty[s]);  // lse / D of this stage no longer read
-          ++n_done;
-          ++it;
         }
       }
       if (!ok) break;
@@ -547,7 +555,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tAcc = tmem + lane_base + (wg == 0 ? L::col_dv() : L::col_dk());
       const float mult = (wg == 0) ? args.drop.keep_scale : args.scale;
       __nv_bfloat16* dst_base = (wg == 0) ? args.dv : args.dk;
-      __nv_bfloat16* dst = dst_base + (static_cast<size_t>(bh) * N + static_cast<size_t>(key)) * D;
+      __nv_bfloat16* dst = dst_base + (static_cast<size_t>(bhk) * N + static_cast<size_t>(key)) * D;
       const bool row_ok = key < N;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -605,7 +613,8 @@ template <int D, bool DROP>
 static cudaError_t launch_dkdv_impl(const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const CUtensorMap& tdo,
                                     const BwdArgs& a, int grid, cudaStream_t stream) {
-  auto kern = fa_bwd_dkdv_kernel<D, DROP>;
+  auto kern = a.mask.Hkv != a.mask.H ? fa_bwd_dkdv_kernel<D, DROP, true>
+                                     : fa_bwd_dkdv_kernel<D, DROP, false>;
   cudaError_t e = set_smem(kern, DkdvLayout<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, kBwdThreads, DkdvLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
@@ -616,7 +625,7 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const BwdArgs& a, int d, bool dropout,
                             int num_sms, cudaStream_t stream) {
   const int n_t = (a.mask.N + kTile - 1) / kTile;
-  const long long units = static_cast<long long>(a.mask.B) * a.mask.H * n_t;
+  const long long units = static_cast<long long>(a.mask.B) * a.mask.Hkv * n_t;  // (K/V head, key tile)
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   if (grid <= 0) return cudaSuccess;
   if (d == 64) return launch_bwd_dkdv_split(tq, tk, tv, tdo, a, d, dropout, num_sms, stream);

@@ -112,7 +112,7 @@ struct DkdvBars {
   uint32_t acc_full, acc_free, drain_a, drain_b;
 };
 
-template <int D, bool DROPOUT>
+template <int D, bool DROPOUT, bool GQA>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_split_kernel(const __grid_constant__ CUtensorMap tm_q,
                              const __grid_constant__ CUtensorMap tm_k,
@@ -129,7 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const MaskParams& mk = args.mask;
   const int N = mk.N;
   const int n_t = (N + kTile - 1) / kTile;
-  const int n_units = mk.B * mk.H * n_t;
+  const int n_units = mk.B * mk.Hkv * n_t;
+  const int G = GQA ? mk.H / mk.Hkv : 1;  // query heads per K/V head
 
   uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
@@ -205,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bh = u / n_t, kt = u % n_t;
-      const int kv_len = kv_len_of(mk, bh / mk.H);
+      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+      const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int kb = unit_count % L::kKVBufs;
       const int kuse = unit_count / L::kKVBufs;
@@ -217,45 +218,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) {
         mbar_expect_tx(bars.kv_full[kb], 2 * T);
-        tma_tile<D>(sKV + (2 * kb) * T, &tm_k, kt * kTile, bh, bars.kv_full[kb]);
-        tma_tile<D>(sKV + (2 * kb + 1) * T, &tm_v, kt * kTile, bh, bars.kv_full[kb]);
+        tma_tile<D>(sKV + (2 * kb) * T, &tm_k, kt * kTile, bhk, bars.kv_full[kb]);
+        tma_tile<D>(sKV + (2 * kb + 1) * T, &tm_v, kt * kTile, bhk, bars.kv_full[kb]);
       }
       ++kv_arms[kb];
-      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
-        while (bits != 0u) {
-          const int qt = chunk * 32 + (__ffs(bits) - 1);
-          bits &= bits - 1;
-          const int s = it % L::kStages;
-          const uint32_t ph = (it / L::kStages) & 1u;
-          if (!mbar_wait_warp(bars.q_empty[s], ph ^ 1u, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
+      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+             ++bh) {  // the query heads sharing this K/V head
+        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          while (bits != 0u) {
+            const int qt = chunk * 32 + (__ffs(bits) - 1);
+            bits &= bits - 1;
+            const int s = it % L::kStages;
+            const uint32_t ph = (it / L::kStages) & 1u;
+            if (!mbar_wait_warp(bars.q_empty[s], ph ^ 1u, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            float4 l4, d4;
+            float* lp = &l4.x;
+            float* dp = &d4.x;
+  #pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int row = qt * kTile + 4 * lane + r;
+              const bool in = row < N;
+              const long long idx = static_cast<long long>(bh) * N + row;
+              lp[r] = -lse2_at(args.lse, idx, in);
+              dp[r] = in ? -args.dsum[idx] : 0.f;
+            }
+            // staged negated: the compute warps add them as packed pairs
+            reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
+            reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
+            if (lane == 0) {
+              mbar_expect_tx(bars.q_full[s], 2 * T);
+              tma_tile<D>(sQ + s * T, &tm_q, qt * kTile, bh, bars.q_full[s]);
+              tma_tile<D>(sDO + s * T, &tm_do, qt * kTile, bh, bars.q_full[s]);
+            } else {
+              mbar_arrive(bars.q_full[s]);
+            }
+            ++q_arms;
+            ++it;
           }
-          float4 l4, d4;
-          float* lp = &l4.x;
-          float* dp = &d4.x;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int row = qt * kTile + 4 * lane + r;
-            const bool in = row < N;
-            const long long idx = static_cast<long long>(bh) * N + row;
-            lp[r] = -lse2_at(args.lse, idx, in);
-            dp[r] = in ? -args.dsum[idx] : 0.f;
-          }
-          // staged negated: the compute warps add them as packed pairs
-          reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
-          reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
-          if (lane == 0) {
-            mbar_expect_tx(bars.q_full[s], 2 * T);
-            tma_tile<D>(sQ + s * T, &tm_q, qt * kTile, bh, bars.q_full[s]);
-            tma_tile<D>(sDO + s * T, &tm_do, qt * kTile, bh, bars.q_full[s]);
-          } else {
-            mbar_arrive(bars.q_full[s]);
-          }
-          ++q_arms;
-          ++it;
         }
       }
     }
@@ -277,11 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bh = u / n_t, kt = u % n_t;
-      const int kv_len = kv_len_of(mk, bh / mk.H);
+      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+      const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int kb = unit_count % L::kKVBufs;
-      (void)bh;
       if (leader &&
           !mbar_wait(bars.kv_full[kb], (unit_count / L::kKVBufs) & 1, tmo, abort_flag)) {
         fail();
@@ -290,34 +293,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       const uint64_t dK = sdesc_sw128(sKV + (2 * kb) * T, 16, 1024);
       const uint64_t dV = sdesc_sw128(sKV + (2 * kb + 1) * T, 16, 1024);
-      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-        const uint32_t vbits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
-        if (leader) {
-          for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
-            const int s = it % L::kStages;
-            const uint32_t ph = (it / L::kStages) & 1u;
-            if (!mbar_wait(bars.q_full[s], ph, tmo, abort_flag) ||
-                (gt > 0 && !mbar_wait(bar_s_ok, sfc++ & 1, tmo, abort_flag))) {
-              ok = false;
-              break;
+      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+             ++bh) {  // the query heads sharing this K/V head
+        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+          const uint32_t vbits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          if (leader) {
+            for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
+              const int s = it % L::kStages;
+              const uint32_t ph = (it / L::kStages) & 1u;
+              if (!mbar_wait(bars.q_full[s], ph, tmo, abort_flag) ||
+                  (gt > 0 && !mbar_wait(bar_s_ok, sfc++ & 1, tmo, abort_flag))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_ss_tile<D>(tmem + L::kColSt, dK, sdesc_sw128(sQ + s * T, 16, 1024));
+              mma_commit(bars.st_full);
+              if (gt > 0 && !mbar_wait(bar_dp_ok, dfc++ & 1, tmo, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_ss_tile<D>(tmem + L::kColDPt, dV, sdesc_sw128(sDO + s * T, 16, 1024));
+              mma_commit(bars.dpt_full);
+              mma_commit(bars.q_empty[s]);
+              ++gt;
+              ++it;
             }
-            tc_fence_after();
-            mma_ss_tile<D>(tmem + L::kColSt, dK, sdesc_sw128(sQ + s * T, 16, 1024));
-            mma_commit(bars.st_full);
-            if (gt > 0 && !mbar_wait(bar_dp_ok, dfc++ & 1, tmo, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            mma_ss_tile<D>(tmem + L::kColDPt, dV, sdesc_sw128(sDO + s * T, 16, 1024));
-            mma_commit(bars.dpt_full);
-            mma_commit(bars.q_empty[s]);
-            ++gt;
-            ++it;
+            if (!ok) fail();
           }
-          if (!ok) fail();
+          ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (leader && ok) mma_commit(bars.kv_empty[kb]);
     }
@@ -333,41 +339,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bh = u / n_t, kt = u % n_t;
-      const int kv_len = kv_len_of(mk, bh / mk.H);
+      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+      const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
       const int n_kv = (kv_len + kTile - 1) / kTile;
-      (void)bh;
       bool first = true;
-      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-        const uint32_t vbits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
-        if (leader) {
-          for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
-            const int s = it % L::kStages;
-            if (!mbar_wait(bars.p_ready, prc++ & 1, tmo, abort_flag) ||
-                (first && unit_count > 0 &&
-                 !mbar_wait(bars.acc_free, (unit_count - 1) & 1, tmo, abort_flag))) {
-              ok = false;
-              break;
+      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+             ++bh) {  // the query heads sharing this K/V head
+        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+          const uint32_t vbits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          if (leader) {
+            for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
+              const int s = it % L::kStages;
+              if (!mbar_wait(bars.p_ready, prc++ & 1, tmo, abort_flag) ||
+                  (first && unit_count > 0 &&
+                   !mbar_wait(bars.acc_free, (unit_count - 1) & 1, tmo, abort_flag))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_ts_tile<D>(tmem + L::kColDV, tmem + L::kColP, L::kPair,
+                             sdesc_sw128(sDO + s * T, 16384, 1024), !first);
+              mma_commit(bars.p_done);
+              if (!mbar_wait(bars.ds_ready, dsc++ & 1, tmo, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_ts_tile<D>(tmem + L::kColDK, tmem + L::kColDS, L::kPair,
+                             sdesc_sw128(sQ + s * T, 16384, 1024), !first);
+              mma_commit(bars.ds_done);
+              mma_commit(bars.q_empty[s]);
+              first = false;
+              ++it;
             }
-            tc_fence_after();
-            mma_ts_tile<D>(tmem + L::kColDV, tmem + L::kColP, L::kPair,
-                           sdesc_sw128(sDO + s * T, 16384, 1024), !first);
-            mma_commit(bars.p_done);
-            if (!mbar_wait(bars.ds_ready, dsc++ & 1, tmo, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            mma_ts_tile<D>(tmem + L::kColDK, tmem + L::kColDS, L::kPair,
-                           sdesc_sw128(sQ + s * T, 16384, 1024), !first);
-            mma_commit(bars.ds_done);
-            mma_commit(bars.q_empty[s]);
-            first = false;
-            ++it;
+            if (!ok) fail();
           }
-          if (!ok) fail();
+          ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (leader && ok) {
         if (first && unit_count > 0 &&
@@ -404,166 +412,169 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bh = u / n_t, kt = u % n_t;
-      const int kv_len = kv_len_of(mk, bh / mk.H);
+      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+      const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int key = kt * kTile + r;
       int n_done = 0;
-      for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
-        while (bits != 0u && ok) {
-          const int qt = chunk * 32 + (__ffs(bits) - 1);
-          bits &= bits - 1;
-          const int s = it % L::kStages;
-          const float* lse_t = lse_s + s * 128 + 32 * wg;
-          const float* dsum_t = dsum_s + s * 128 + 32 * wg;
-          const int q0 = qt * kTile + 32 * wg;  // first query column of this warpgroup
-          // Dropout keep bytes (0x00 / 0xFF) of this thread's key for the 32 query
-          // columns, four per word: column c is byte c & 3 of bm[c >> 2].
-          uint32_t bm[8];
-          if constexpr (DROPOUT) {
-            // The warp's 32 keys are two 16-key Philox groups; for each of the 32
-            // queries both groups are generated (two blocks per lane) and each
-            // lane then reads its own key's byte.
-            const uint32_t kgroup0 = static_cast<uint32_t>(kt * kTile + quad * 32) >> 4;
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              const int idx = lane + 32 * m;
-              const int c = idx >> 1, gs = idx & 1;
-              const uint32_t rowg = static_cast<uint32_t>(bh) * static_cast<uint32_t>(N) +
-                                    static_cast<uint32_t>(q0 + c);
-              reinterpret_cast<uint4*>(drop_scratch)[c * 2 + gs] =
-                  dropout_keep16(args.drop, rowg, kgroup0 + gs);
+      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+             ++bh) {  // the query heads sharing this K/V head
+        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          while (bits != 0u && ok) {
+            const int qt = chunk * 32 + (__ffs(bits) - 1);
+            bits &= bits - 1;
+            const int s = it % L::kStages;
+            const float* lse_t = lse_s + s * 128 + 32 * wg;
+            const float* dsum_t = dsum_s + s * 128 + 32 * wg;
+            const int q0 = qt * kTile + 32 * wg;  // first query column of this warpgroup
+            // Dropout keep bytes (0x00 / 0xFF) of this thread's key for the 32 query
+            // columns, four per word: column c is byte c & 3 of bm[c >> 2].
+            uint32_t bm[8];
+            if constexpr (DROPOUT) {
+              // The warp's 32 keys are two 16-key Philox groups; for each of the 32
+              // queries both groups are generated (two blocks per lane) and each
+              // lane then reads its own key's byte.
+              const uint32_t kgroup0 = static_cast<uint32_t>(kt * kTile + quad * 32) >> 4;
+  #pragma unroll
+              for (int m = 0; m < 2; ++m) {
+                const int idx = lane + 32 * m;
+                const int c = idx >> 1, gs = idx & 1;
+                const uint32_t rowg = static_cast<uint32_t>(bh) * static_cast<uint32_t>(N) +
+                                      static_cast<uint32_t>(q0 + c);
+                reinterpret_cast<uint4*>(drop_scratch)[c * 2 + gs] =
+                    dropout_keep16(args.drop, rowg, kgroup0 + gs);
+              }
+              __syncwarp();
+              // this lane's key is byte (lane & 3) of word (lane & 15) >> 2 of the
+              // block of its 16-key group: gather it for four columns at a time
+              const uint32_t kb = static_cast<uint32_t>(lane & 3);
+              const uint32_t sel2 = kb | ((4u + kb) << 4);  // byte kb of a, then byte kb of b
+              const uint32_t* wcol = drop_scratch + (lane >> 4) * 4 + ((lane & 15) >> 2);
+  #pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t t0 = prmt(wcol[(4 * k + 0) * 8], wcol[(4 * k + 1) * 8], sel2);
+                const uint32_t t1 = prmt(wcol[(4 * k + 2) * 8], wcol[(4 * k + 3) * 8], sel2);
+                bm[k] = prmt(t0, t1, 0x5410u);
+              }
+              __syncwarp();
+            }
+            // ---- P^T = exp2(S^T c - lse2) for 32 query columns
+            if (!mbar_wait_warp(bars.st_full, stc++ & 1, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            float p[32];  // P^T, fp32, kept until dS^T is formed
+            {
+              uint32_t sr[32];
+              tmem_ld32(tSt, sr);
+              tmem_ld_wait();
+              if constexpr (L::kSepBuf) {
+                tc_fence_before();
+                mbar_arrive(bars.st_free);
+              }
+              const uint64_t c2 = f2_pack(c_log2, c_log2);
+  #pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4) {
+                const ulonglong2 nl = reinterpret_cast<const ulonglong2*>(lse_t)[c4];  // -lse2 pairs
+  #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int c = 4 * c4 + 2 * h;
+                  float x0, x1;
+                  f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2,
+                                   h ? nl.y : nl.x),
+                            x0, x1);
+                  p[c] = ex2_approx(x0);
+                  p[c + 1] = ex2_approx(x1);
+                }
+              }
+            }
+            if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
+              const bool key_ok = key < kv_len;
+  #pragma unroll
+              for (int c = 0; c < 32; ++c)
+                p[c] = (key_ok && (!mk.causal || key <= q0 + c)) ? p[c] : 0.f;
+            }
+            {
+              uint32_t pk[16];  // dropped copy for dV
+  #pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                uint32_t pp = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+                if constexpr (DROPOUT) pp &= prmt(bm[c >> 1], 0u, (c & 1) ? 0x3322u : 0x1100u);
+                pk[c] = pp;
+              }
+              if constexpr (L::kSepBuf) {
+                if (gt > 0) {  // the previous dV has finished reading the P^T buffer
+                  if (!mbar_wait_warp(bars.p_done, pdc++ & 1, tmo, abort_flag)) {
+                    fail();
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                }
+              }
+              tmem_st16(tP, pk);
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(bars.p_ready);
+            }
+            // ---- dS^T = P^T (Z dP^T / (1 - p) - D)
+            if (!mbar_wait_warp(bars.dpt_full, dpc++ & 1, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            {
+              uint32_t dr[32];
+              tmem_ld32(tDPt, dr);
+              tmem_ld_wait();
+              if constexpr (L::kSepBuf) {
+                tc_fence_before();
+                mbar_arrive(bars.dpt_free);
+              }
+              uint32_t pk[16];
+  #pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4) {
+                const ulonglong2 nd = reinterpret_cast<const ulonglong2*>(dsum_t)[c4];  // -D pairs
+  #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int c = 4 * c4 + 2 * h;
+                  uint32_t dp0 = dr[c], dp1 = dr[c + 1];
+                  if constexpr (DROPOUT) {  // keep byte -> all-ones / all-zeros lane mask
+                    dp0 &= prmt(bm[c >> 2], 0u, (8u | (c & 3)) * 0x1111u);
+                    dp1 &= prmt(bm[c >> 2], 0u, (8u | ((c + 1) & 3)) * 0x1111u);
+                  }
+                  const uint64_t t = f2_fma(ks2, f2_pack(__uint_as_float(dp0), __uint_as_float(dp1)),
+                                            h ? nd.y : nd.x);
+                  float a0, a1;
+                  f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), a0, a1);
+                  pk[2 * c4 + h] = pack_bf16x2(a0, a1);
+                }
+              }
+              if constexpr (L::kSepBuf) {
+                if (gt > 0) {  // the previous dK has finished reading the dS^T buffer
+                  if (!mbar_wait_warp(bars.ds_done, dsc++ & 1, tmo, abort_flag)) {
+                    fail();
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                }
+              }
+              tmem_st16(tDS, pk);
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(bars.ds_ready);
             }
             __syncwarp();
-            // this lane's key is byte (lane & 3) of word (lane & 15) >> 2 of the
-            // block of its 16-key group: gather it for four columns at a time
-            const uint32_t kb = static_cast<uint32_t>(lane & 3);
-            const uint32_t sel2 = kb | ((4u + kb) << 4);  // byte kb of a, then byte kb of b
-            const uint32_t* wcol = drop_scratch + (lane >> 4) * 4 + ((lane & 15) >> 2);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t t0 = prmt(wcol[(4 * k + 0) * 8], wcol[(4 * k + 1) * 8], sel2);
-              const uint32_t t1 = prmt(wcol[(4 * k + 2) * 8], wcol[(4 * k + 3) * 8], sel2);
-              bm[k] = prmt(t0, t1, 0x5410u);
-            }
-            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.q_empty[s]);  // lse / D of this stage no longer read
+            ++n_done;
+            ++gt;
+            ++it;
           }
-          // ---- P^T = exp2(S^T c - lse2) for 32 query columns
-          if (!mbar_wait_warp(bars.st_full, stc++ & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          float p[32];  // P^T, fp32, kept until dS^T is formed
-          {
-            uint32_t sr[32];
-            tmem_ld32(tSt, sr);
-            tmem_ld_wait();
-            if constexpr (L::kSepBuf) {
-              tc_fence_before();
-              mbar_arrive(bars.st_free);
-            }
-            const uint64_t c2 = f2_pack(c_log2, c_log2);
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const ulonglong2 nl = reinterpret_cast<const ulonglong2*>(lse_t)[c4];  // -lse2 pairs
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int c = 4 * c4 + 2 * h;
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2,
-                                 h ? nl.y : nl.x),
-                          x0, x1);
-                p[c] = ex2_approx(x0);
-                p[c + 1] = ex2_approx(x1);
-              }
-            }
-          }
-          if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
-            const bool key_ok = key < kv_len;
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              p[c] = (key_ok && (!mk.causal || key <= q0 + c)) ? p[c] : 0.f;
-          }
-          {
-            uint32_t pk[16];  // dropped copy for dV
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              uint32_t pp = pack_bf16x2(p[2 * c], p[2 * c + 1]);
-              if constexpr (DROPOUT) pp &= prmt(bm[c >> 1], 0u, (c & 1) ? 0x3322u : 0x1100u);
-              pk[c] = pp;
-            }
-            if constexpr (L::kSepBuf) {
-              if (gt > 0) {  // the previous dV has finished reading the P^T buffer
-                if (!mbar_wait_warp(bars.p_done, pdc++ & 1, tmo, abort_flag)) {
-                  fail();
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-              }
-            }
-            tmem_st16(tP, pk);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bars.p_ready);
-          }
-          // ---- dS^T = P^T (Z dP^T / (1 - p) - D)
-          if (!mbar_wait_warp(bars.dpt_full, dpc++ & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          {
-            uint32_t dr[32];
-            tmem_ld32(tDPt, dr);
-            tmem_ld_wait();
-            if constexpr (L::kSepBuf) {
-              tc_fence_before();
-              mbar_arrive(bars.dpt_free);
-            }
-            uint32_t pk[16];
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const ulonglong2 nd = reinterpret_cast<const ulonglong2*>(dsum_t)[c4];  // -D pairs
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int c = 4 * c4 + 2 * h;
-                uint32_t dp0 = dr[c], dp1 = dr[c + 1];
-                if constexpr (DROPOUT) {  // keep byte -> all-ones / all-zeros lane mask
-                  dp0 &= prmt(bm[c >> 2], 0u, (8u | (c & 3)) * 0x1111u);
-                  dp1 &= prmt(bm[c >> 2], 0u, (8u | ((c + 1) & 3)) * 0x1111u);
-                }
-                const uint64_t t = f2_fma(ks2, f2_pack(__uint_as_float(dp0), __uint_as_float(dp1)),
-                                          h ? nd.y : nd.x);
-                float a0, a1;
-                f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t), a0, a1);
-                pk[2 * c4 + h] = pack_bf16x2(a0, a1);
-              }
-            }
-            if constexpr (L::kSepBuf) {
-              if (gt > 0) {  // the previous dK has finished reading the dS^T buffer
-                if (!mbar_wait_warp(bars.ds_done, dsc++ & 1, tmo, abort_flag)) {
-                  fail();
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-              }
-            }
-            tmem_st16(tDS, pk);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bars.ds_ready);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars.q_empty[s]);  // lse / D of this stage no longer read
-          ++n_done;
-          ++gt;
-          ++it;
         }
       }
       if (!ok) break;
@@ -580,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem + lane_base + (is_dv ? L::kColDV : L::kColDK) + kHalf * (wg & 1);
       const float mult = is_dv ? args.drop.keep_scale : args.scale;
       __nv_bfloat16* dst = (is_dv ? args.dv : args.dk) +
-                           (static_cast<size_t>(bh) * N + static_cast<size_t>(key)) * D +
+                           (static_cast<size_t>(bhk) * N + static_cast<size_t>(key)) * D +
                            kHalf * (wg & 1);
 #pragma unroll
       for (int c = 0; c < kHalf / 32; ++c) {
@@ -751,6 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       int bh, qt;
       unit_coords(u, bh, qt);
+      const int kvh = kv_head(mk, bh);  // K/V head of this query head
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int jmax = kv_limit(qt, n_kv);
@@ -779,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             mbar_expect_tx(bars.k_full[ks], T);
-            tma_tile<D>(sK + ks * T, &tm_k, j * kTile, bh, bars.k_full[ks]);
+            tma_tile<D>(sK + ks * T, &tm_k, j * kTile, kvh, bars.k_full[ks]);
           }
           ++k_arms;
           if (!mbar_wait_warp(bars.v_empty[vs], ((it / L::kVStages) & 1u) ^ 1u, tmo, abort_flag)) {
@@ -789,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             mbar_expect_tx(bars.v_full[vs], T);
-            tma_tile<D>(sV + vs * T, &tm_v, j * kTile, bh, bars.v_full[vs]);
+            tma_tile<D>(sV + vs * T, &tm_v, j * kTile, kvh, bars.v_full[vs]);
           }
           ++v_arms;
           ++it;
@@ -1121,7 +1133,11 @@ template <int D>
 cudaError_t launch_dkdv_split_d(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
                                 bool dropout, int grid, cudaStream_t stream) {
-  auto kern = dropout ? fa_bwd_dkdv_split_kernel<D, true> : fa_bwd_dkdv_split_kernel<D, false>;
+  const bool gqa = a.mask.Hkv != a.mask.H;
+  auto kern = dropout ? (gqa ? fa_bwd_dkdv_split_kernel<D, true, true>
+                             : fa_bwd_dkdv_split_kernel<D, true, false>)
+                      : (gqa ? fa_bwd_dkdv_split_kernel<D, false, true>
+                             : fa_bwd_dkdv_split_kernel<D, false, false>);
   cudaError_t e = set_smem_split(kern, DkdvL<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, DkdvL<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
@@ -1145,11 +1161,11 @@ cudaError_t launch_bwd_dkdv_split(const CUtensorMap& tq, const CUtensorMap& tk,
                                   const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
                                   int d, bool dropout, int num_sms, cudaStream_t stream) {
   const int n_t = (a.mask.N + kTile - 1) / kTile;
-  const long long units = static_cast<long long>(a.mask.B) * a.mask.H * n_t;
+  const long long units = static_cast<long long>(a.mask.B) * a.mask.Hkv * n_t;  // (K/V head, key tile)
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   if (grid <= 0) return cudaSuccess;
-  return d == 64 ? launch_dkdv_split_d<64>(tq, tk, tv, tdo, a, dropout, grid, stream)
-                 : launch_dkdv_split_d<128>(tq, tk, tv, tdo, a, dropout, grid, stream);
+  if (d != 64) return cudaErrorInvalidValue;  // head dimension 128 runs the single-issuer kernel
+  return launch_dkdv_split_d<64>(tq, tk, tv, tdo, a, dropout, grid, stream);
 }
 
 cudaError_t launch_bwd_dq_split(const CUtensorMap& tq, const CUtensorMap& tk,

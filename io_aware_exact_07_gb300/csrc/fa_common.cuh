@@ -19,6 +19,7 @@ constexpr unsigned kStatusTimeout = 5u;
 
 struct MaskParams {
   int B, H, N;
+  int Hkv;                      // K/V heads (H for per-head attention; H / Hkv query heads share one)
   int nb;                       // ceil(N / 128): tiles per side, block-mask row length
   int causal;
   const uint8_t* block_mask;    // [nb, nb] or null
@@ -43,6 +44,22 @@ struct SyncParams {
 
 __device__ __forceinline__ void record_error(unsigned int* status, unsigned code) {
   atomicCAS(status, 0u, code);
+}
+
+// K/V head of query head bh = b*H + h: grouped-query attention gives the H / Hkv
+// query heads h of a group the K/V head h / (H / Hkv) of the same batch row.
+__device__ __forceinline__ int kv_head(const MaskParams& m, int bh) {
+  const int b = bh / m.H, h = bh - b * m.H;
+  return b * m.Hkv + h / (m.H / m.Hkv);
+}
+
+// First query head bh = b*H + h of the group that shares K/V head bhk = b*Hkv + j;
+// the group is the G = H / Hkv consecutive heads from there. With one query head
+// per K/V head (GQA false) that is bhk itself.
+template <bool GQA>
+__device__ __forceinline__ int group_first_head(const MaskParams& m, int bhk) {
+  if constexpr (!GQA) return bhk;
+  return (bhk / m.Hkv) * m.H + (bhk % m.Hkv) * (m.H / m.Hkv);
 }
 
 // Number of valid keys of batch b (key padding clamps to [0, N]).

@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
+      const int kvh = kv_head(mk, uc.bh);  // K/V head of this query head
       const int kv_len = kv_len_of(mk, uc.b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       int jmax = n_kv;
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (lane == 0) {
             mbar_expect_tx(bars.k_full[s], L::kTileBytes);
             for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(sK + s * L::kTileBytes + c * 16384, &tm_k, c * 64, j * kTile, uc.bh,
+              tma_load_3d(sK + s * L::kTileBytes + c * 16384, &tm_k, c * 64, j * kTile, kvh,
                           bars.k_full[s]);
           }
           ++k_arms;
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (lane == 0) {
             mbar_expect_tx(bars.v_full[s], L::kTileBytes);
             for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(sV + s * L::kTileBytes + c * 16384, &tm_v, c * 64, j * kTile, uc.bh,
+              tma_load_3d(sV + s * L::kTileBytes + c * 16384, &tm_v, c * 64, j * kTile, kvh,
                           bars.v_full[s]);
           }
           ++v_arms;

@@ -46,7 +46,8 @@ cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const CUtensorMap& tdo, const BwdArgs& a, int d, bool dropout,
                           int num_sms, cudaStream_t stream);
 
-// Two-issuer backward kernels (fa_bwd_split.cu), d = 64 or 128.
+// Two-issuer backward kernels (fa_bwd_split.cu): dK/dV at d = 64 (d = 128 runs the
+// single-issuer kernel of fa_bwd.cu), dQ at d = 64 or 128.
 cudaError_t launch_bwd_dkdv_split(const CUtensorMap& tq, const CUtensorMap& tk,
                                   const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
                                   int d, bool dropout, int num_sms, cudaStream_t stream);

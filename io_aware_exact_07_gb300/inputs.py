@@ -5,8 +5,9 @@ it holds none of the attention arithmetic. Both the GPU path and the CPU
 oracle consume what it produces.
 
 Recipe (one CPU ``torch.Generator`` seeded with ``seed``):
-  Q, K, V, dO drawn in that order as ``randn(B, H, N, d)`` in fp32, then
-  rounded to bf16; for the key-padding workload the per-sequence valid key
+  Q, K, V, dO drawn in that order as ``randn(B, H, N, d)`` in fp32 (K and V
+  with H_kv heads for grouped-query attention), then rounded to bf16; for the
+  key-padding workload the per-sequence valid key
   lengths are drawn next as ``randint(lo, hi + 1, (B,))``. The dropout Philox
   stream uses (seed, offset) = (0, 0). The block-sparse workload's mask is the
   deterministic butterfly pattern built by the library itself.
@@ -31,7 +32,12 @@ class Workload:
     padding: tuple | None = None  # (lo, hi) inclusive range of valid key lengths
     butterfly: bool = False
     seed: int = 0
+    Hkv: int | None = None  # K/V heads (grouped-query attention); None: one per query head
     description: str = field(default="", compare=False)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.Hkv is None else self.Hkv
 
     @property
     def scale(self) -> float:
@@ -53,17 +59,25 @@ LONG_D128 = Workload("long_16k_d128", 1, 16, 16384, 128,
 SPARSE = Workload("butterfly_16k", 4, 16, 16384, 64, butterfly=True,
                   description="B=4 H=16 N=16384 d=64, butterfly block mask, 128x128 blocks")
 
-ALL = {w.name: w for w in (TINY, GPT2_MEDIUM, CAUSAL, LONG_D64, LONG_D128, SPARSE)}
+# Grouped-query attention (K/V heads shared by query heads, which the page on
+# FlashAttention and its successors names as a further cut of K/V reads),
+# measured beyond the five workloads: the causal decoder shape with 4 query
+# heads per K/V head.
+GQA_CAUSAL = Workload("gqa_causal_4k", 8, 32, 4096, 128, causal=True, Hkv=8,
+                      description="B=8 H=32 H_kv=8 N=4096 d=128, causal, grouped K/V heads")
+
+ALL = {w.name: w for w in (TINY, GPT2_MEDIUM, CAUSAL, LONG_D64, LONG_D128, SPARSE, GQA_CAUSAL)}
 
 
 def draw(w: Workload, with_grad: bool = True):
     """Return dict with bf16 CPU tensors q, k, v, (do) and int32 seqlens (or None)."""
     g = torch.Generator().manual_seed(w.seed)
-    shape = (w.B, w.H, w.N, w.d)
     out = {}
     names = ("q", "k", "v", "do") if with_grad else ("q", "k", "v")
     for name in names:
-        out[name] = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+        heads = w.kv_heads if name in ("k", "v") else w.H
+        out[name] = torch.randn((w.B, heads, w.N, w.d), generator=g,
+                                dtype=torch.float32).to(torch.bfloat16)
     if w.padding is not None:
         lo, hi = w.padding
         out["seqlens"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int64).to(

@@ -211,8 +211,10 @@ def _group(H: int, Hkv: int) -> int:
 
 
 def fwd_gqa(q, k, v, scale, **kw):
-    """Grouped-query attention forward (the K/V-head sharing the cross-paper
-    synthesis page lists among FlashAttention's successors): q [B, H, N, d],
+    """Grouped-query attention forward (K/V heads shared by several query heads,
+    which the page "Attention Kernel: FlashAttention 与它的后继者", section on
+    FlashAttention's IO-aware insight, names as a further cut of K/V reads):
+    q [B, H, N, d],
     k and v [B, H_kv, N, d] with H a multiple of H_kv; query head h of batch b
     attends with K/V head h // (H / H_kv). Written out from that definition:
     every query head gets its group's K/V and the per-head forward above runs
