@@ -236,3 +236,45 @@ def bwd_gqa(q, k, v, dout, scale, **kw):
     dk = dk.reshape(B, Hkv, G, N, d).sum(axis=2)
     dv = dv.reshape(B, Hkv, G, N, d).sum(axis=2)
     return dq, dk, dv, D
+
+
+def fwd_decode(q, k, v, scale, causal=False, seqlens_k=None, heads=None):
+    """Attention of a short block of new query rows over a key/value cache, in
+    fp64: the decode case that the page "FlashAttention — L3 Cross-Paper
+    Synthesis" (section 3, the attack surface) names as left unoptimised,
+    where one or a few query rows read a long cache.
+
+    q [B, H, Nq, d]; k, v [B, H_kv, Nk, d] with H a multiple of H_kv (query
+    head h reads K/V head h // (H / H_kv)); seqlens_k [B]: valid cache length
+    L_b of each batch row (default Nk, clamped to [0, Nk]). The Nq query rows
+    are the last Nq positions of the sequence: row i sits at position
+    L_b - Nq + i. Without causal it sees keys j < L_b; with causal it sees
+    j <= L_b - Nq + i as well. Written out row by row from the definition of
+    softmax attention: scores scale * q . k_j over the allowed keys, their
+    softmax, the weighted sum of V rows, and lse = log of the softmax
+    denominator. A row with no allowed key has O = 0, lse = -inf.
+
+    heads: optional list of (b, h) to compute; the others stay O = 0,
+    lse = -inf. Returns (o [B, H, Nq, d], lse [B, H, Nq])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    G = _group(H, Hkv)
+    o = np.zeros((B, H, Nq, d))
+    lse = np.full((B, H, Nq), -np.inf)
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads:
+        L = Nk if seqlens_k is None else min(max(int(seqlens_k[b]), 0), Nk)
+        kh, vh = k[b, h // G], v[b, h // G]
+        for i in range(Nq):
+            n = min(L, L - Nq + i + 1) if causal else L  # allowed keys are j < n
+            if n <= 0:
+                continue
+            s = scale * (kh[:n] @ q[b, h, i])
+            m = s.max()
+            e = np.exp(s - m)
+            den = e.sum()
+            o[b, h, i] = (e @ vh[:n]) / den
+            lse[b, h, i] = m + np.log(den)
+    return o, lse
