@@ -12,6 +12,11 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
 Under torchrun every rank runs the same workload on its own GPU (the path
 shards by heads and batches; there is no data-path collective) and rank 0
 prints one JSON line with the whole-job throughput.
+
+``--workload decode_16k`` measures the forward-only short-query kernel
+(fa_decode) instead: one step is one decode call, and the metric is the
+algorithmic HBM bytes it must move per second (K/V cache rows each sequence
+sees, Q, O, lse) against the measured copy bandwidth.
 """
 from __future__ import annotations
 
@@ -501,22 +506,204 @@ def run_reference(args, w):
     }
 
 
+# ------------------------------------------------------------ decode workload
+
+DECODE_METRIC = "decode attention (fa_decode): algorithmic HBM GB/s"
+
+
+def decode_bytes(w, seqlens, heads=None):
+    """Bytes fa_decode must move: the visible K/V cache rows of every K/V head
+    (bf16 K and V), Q read, O written (bf16) and lse (fp32). heads: optional
+    list of (b, K/V head) groups to count instead of all."""
+    G = w.H // w.Hkv
+    groups = heads if heads is not None else [(b, j) for b in range(w.B) for j in range(w.Hkv)]
+    total = 0
+    for b, _ in groups:
+        L = w.Nk if seqlens is None else min(max(int(seqlens[b]), 0), w.Nk)
+        total += 2 * L * w.d * 2 + G * w.Nq * (2 * w.d * 2 + 4)
+    return total
+
+
+def run_decode(args, w):
+    world, rank, local, pg = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import io_aware_exact_07_gb300 as fa
+    x = inputs.draw_decode(w)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    sl = None if x["seqlens"] is None else x["seqlens"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    ws_bytes = fa.fa_decode_workspace_size(w.B, w.H, w.Hkv, w.Nq, w.Nk, w.d, 0)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    byts = decode_bytes(w, None if x["seqlens"] is None else x["seqlens"].tolist())
+
+    def call():
+        st = fa.fa_decode(q, k, v, o, lse, w.B, w.H, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal,
+                          sl, 0, ws, ws_bytes)
+        if st != 0:
+            raise RuntimeError(f"fa_decode failed with status {st}")
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0, "device-side error during warm-up"
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for e0, e1 in evs:
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(pg)
+    elapsed = max_over_ranks(pg, start.elapsed_time(end) / 1e3)
+    t_call = statistics.mean(e0.elapsed_time(e1) / 1e3 for e0, e1 in evs)
+    assert fa.fa_device_status() == 0, "device-side error during the timed region"
+
+    e2e = None
+    if not args.no_e2e:
+        # per step: the new query rows in from pinned host memory, O and lse out;
+        # the K/V cache is device-resident state, as in serving
+        hq = x["q"].pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        n = max(3, min(args.steps, 50))
+
+        def one():
+            q.copy_(hq, non_blocking=True)
+            call()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        one()
+        torch.cuda.synchronize()
+        barrier(pg)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n):
+            one()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        secs = max_over_ranks(pg, a0.elapsed_time(a1) / 1e3)
+        e2e = {"value": byts * n * world / secs / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hq.numel() * hq.element_size(),
+               "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
+               "steps": n}
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return None
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    value = byts * args.steps * world / elapsed / 1e9
+    ach = byts / t_call / 1e9
+    launches = 2 if ws_bytes > 0 else 1
+    result = {
+        "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q, K/V cache; no dataset)",
+        "config": {"workload": w.name, "description": w.description, "B": w.B, "H": w.H,
+                   "H_kv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+                   "cache_lengths": w.lengths, "bytes_per_step": byts,
+                   "tokens_per_s": w.B * w.Nq * args.steps * world / elapsed,
+                   "l2": "K/V cache larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world} (no collective)"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                     "frac": ach / hbm, "traffic": ncu_traffic("decode", w.name),
+                     "kernel": "fa_decode call (main kernel + combine)",
+                     "peak_source": f"{peak_src} (hbm_gbs)"},
+        "e2e": e2e,
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        result["cpu_baseline"] = decode_cpu_baseline(w, x)
+        result["cpu_baseline"].pop("seconds", None)
+    if pg is not None:
+        pg.destroy_process_group()
+    return result
+
+
+def decode_cpu_baseline(w, x, budget_s=12.0):
+    """The fp64 oracle's fwd_decode timed on whole K/V groups (all G query heads
+    of a K/V head), as many as fit the time budget."""
+    import oracle
+    G = w.H // w.Hkv
+    f64 = {n: x[n].double().numpy() for n in ("q", "k", "v")}
+    sl = None if x["seqlens"] is None else x["seqlens"].numpy()
+    groups = [(b, j) for b in range(w.B) for j in range(w.Hkv)]
+
+    def run(gs):
+        heads = [(b, j * G + g) for b, j in gs for g in range(G)]
+        t0 = time.perf_counter()
+        oracle.fwd_decode(f64["q"], f64["k"], f64["v"], w.scale, causal=w.causal, seqlens_k=sl,
+                          heads=heads)
+        return time.perf_counter() - t0
+
+    t1 = run(groups[:1])
+    n = int(max(1, min(len(groups), budget_s / max(t1, 1e-6))))
+    t = run(groups[:n]) if n > 1 else t1
+    byts = decode_bytes(w, sl, groups[:n])
+    return {"value": byts / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {len(groups)} K/V groups of {w.name} (all their query heads), "
+                      f"fp64 numpy, {t:.1f} s", "seconds": t}
+
+
+def run_decode_reference(args, w):
+    """The fp64 oracle's fwd_decode on the host, one K/V group per step."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    x = inputs.draw_decode(w)
+    cb = None
+    for _ in range(args.warmup):
+        decode_cpu_baseline(w, x, budget_s=0.0)
+    secs = 0.0
+    for _ in range(args.steps):
+        cb = decode_cpu_baseline(w, x, budget_s=0.0)  # one group per step
+        secs += cb["seconds"]
+    byts = decode_bytes(w, None if x["seqlens"] is None else x["seqlens"].numpy(), [(0, 0)])
+    value = byts * args.steps / secs / 1e9
+    sample = f"K/V group (0, 0) of {w.name} (all its query heads) per step, fp64 numpy"
+    return {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), same inputs)",
+        "config": {"workload": w.name, "description": w.description, "bytes_per_step": byts},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.ALL))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(inputs.ALL) + [inputs.DECODE.name])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
-    w = inputs.ALL[args.workload]
-    if args.impl == "reference":
-        res = run_reference(args, w)
+    if args.workload == inputs.DECODE.name:
+        w = inputs.DECODE
+        res = run_decode_reference(args, w) if args.impl == "reference" else run_decode(args, w)
     else:
-        res = run_ours(args, w)
+        w = inputs.ALL[args.workload]
+        res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if res is not None:
         print(json.dumps(res), flush=True)
 

@@ -156,6 +156,40 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          uint64_t seed, uint64_t offset, const uint8_t* block_mask,
                          const int32_t* seqlens_k, void* stream);
 
+/* Short-query attention over a key/value cache (decode): Nq new query rows
+ * per head attend over a cache of Nk keys, forward only. The page
+ * "FlashAttention — L3 Cross-Paper Synthesis" (section 3) names this case,
+ * bound by reading the K/V cache from HBM, as one the FlashAttention kernels
+ * leave unoptimised. Query rows are the last Nq positions of each sequence:
+ * row i of batch b sits at position L_b - Nq + i, where L_b = seqlens_k[b]
+ * (clamped to [0, Nk]; Nk when seqlens_k is null). Without causal it sees
+ * cache keys j < L_b; with causal, j <= L_b - Nq + i as well. A row that
+ * sees no key gets O = 0 and lse = -inf.
+ *   q, o:          bf16 [B, H, Nq, d], contiguous, 16-byte aligned (device)
+ *   k_cache, v_cache: bf16 [B, H_kv, Nk, d], contiguous, 16-byte aligned
+ *   lse:           fp32 [B, H, Nq], natural log (device)
+ *   seqlens_k:     int32 [B] (device) or NULL
+ *   H a multiple of H_kv (query head h reads K/V head h / (H / H_kv)), with
+ *   (H / H_kv) * Nq <= 128: the query rows of a K/V group form one tile, so
+ *   every K/V tile is read from HBM once per group. d = 64 or 128.
+ *   num_ctas: number of CTAs the (K/V head, key tile) pairs are divided
+ *   among; 0 = one per SM. A K/V head cut between two CTAs is finished by a
+ *   second, small kernel that merges the pieces' normalised outputs with the
+ *   online softmax's merge rule; it needs the caller's workspace of
+ *   fa_decode_workspace_size(...) bytes (16-byte aligned, device; 0 when no
+ *   head is cut, and then workspace may be NULL). The result does not depend
+ *   on num_ctas beyond fp32 rounding of the merge.
+ * Errors: FA_ERR_INVALID_ARG (null or unaligned pointers, sizes < 1, H not a
+ * multiple of H_kv, scale not positive and finite, num_ctas < 0),
+ * FA_ERR_UNSUPPORTED (d not 64/128, (H / H_kv) * Nq > 128, not an sm_100-family
+ * GPU), FA_ERR_WORKSPACE, FA_ERR_CUDA. Asynchronous on `stream`; nothing is
+ * allocated. */
+size_t fa_decode_workspace_size(int B, int H, int H_kv, int Nq, int Nk, int d, int num_ctas);
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
+                    const int32_t* seqlens_k, int num_ctas, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
 /* Quantised dropout threshold round(256 p) used by fa_fwd / fa_bwd (-1 if p is
  * outside [0, 1)). The effective dropout rate is fa_dropout_p8(p) / 256. */
 int fa_dropout_p8(float dropout_p);

@@ -8,7 +8,8 @@ computation runs in the library's CUDA kernels. There is no CPU fallback: if
 the library is missing or fails to load, calls raise.
 
 ``fwd`` / ``bwd`` are conveniences that allocate the outputs (and the backward
-workspace) with torch and call ``fa_fwd`` / ``fa_bwd``.
+workspace) with torch and call ``fa_fwd`` / ``fa_bwd``; ``decode`` does the
+same for ``fa_decode`` (short query blocks over a K/V cache).
 """
 from __future__ import annotations
 
@@ -32,7 +33,7 @@ FA_ERR_TIMEOUT = 5
 # Symbols declared in include/fa.h.
 EXPORTS = (
     "fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_workspace_size", "fa_bwd_preprocess",
-    "fa_bwd_dkdv", "fa_bwd_dq",
+    "fa_bwd_dkdv", "fa_bwd_dq", "fa_decode", "fa_decode_workspace_size",
     "fa_bwd_noalloc", "fa_dropout_p8", "fa_debug_dropout_keep",
     "fa_debug_philox", "fa_butterfly_mask", "fa_device_status", "fa_set_wait_timeout_ns",
     "fa_test_inject_stall", "fa_status_string",
@@ -88,6 +89,10 @@ def load(build_if_missing: bool = False):
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f,
                                        u64, u64, vp, vp, vp]
         lib.fa_bwd_noalloc.restype = i
+        lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        lib.fa_decode_workspace_size.restype = sz
+        lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
+        lib.fa_decode.restype = i
         lib.fa_dropout_p8.argtypes = [f]
         lib.fa_dropout_p8.restype = i
         lib.fa_debug_dropout_keep.argtypes = [vp, i, i, i, f, u64, u64, vp]
@@ -236,6 +241,20 @@ def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal=
                                  sl, _stream(stream))
 
 
+def fa_decode_workspace_size(B, H, H_kv, Nq, Nk, d, num_ctas=0) -> int:
+    return int(load().fa_decode_workspace_size(B, H, H_kv, Nq, Nk, d, num_ctas))
+
+
+def fa_decode(q, k_cache, v_cache, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal=False,
+              seqlens_k=None, num_ctas=0, workspace=None, workspace_bytes=0, stream=None) -> int:
+    if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda
+                                  or not seqlens_k.is_contiguous()):
+        raise ValueError("seqlens_k must be a contiguous int32 CUDA tensor")
+    return load().fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, H, H_kv,
+                            Nq, Nk, d, float(scale), int(bool(causal)), _ptr(seqlens_k),
+                            int(num_ctas), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
 def fa_dropout_p8(p: float) -> int:
     return int(load().fa_dropout_p8(float(p)))
 
@@ -314,3 +333,25 @@ def bwd(q, k, v, o, dout, lse, scale=None, causal=False, dropout_p=0.0, seed=0, 
                         workspace.numel(), stream)
     _check(st, "fa_bwd")
     return dq, dk, dv
+
+
+def decode(q, k_cache, v_cache, scale=None, causal=False, seqlens_k=None, num_ctas=0,
+           stream=None):
+    """Allocate O, lse (and the workspace, if the split needs one) with torch and
+    run fa_decode: q [B, H, Nq, d] over k_cache, v_cache [B, H_kv, Nk, d].
+    Returns (o, lse)."""
+    _check_qkv(q, k_cache, v_cache)
+    B, H, Nq, d = q.shape
+    _, Hkv, Nk, _ = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.shape[0] != B or \
+            k_cache.shape[3] != d:
+        raise ValueError("k_cache and v_cache must be [B, H_kv, Nk, d] like q's B and d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ws_bytes = fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d, num_ctas)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
+    _check(fa_decode(q, k_cache, v_cache, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, seqlens_k,
+                     num_ctas, ws, ws_bytes, stream), "fa_decode")
+    return o, lse

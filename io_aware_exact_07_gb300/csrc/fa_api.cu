@@ -376,6 +376,103 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                 offset, block_mask, seqlens_k, scratch, kNoAllocMaxRows * sizeof(float), stream);
 }
 
+// Work split of fa_decode: the (K/V head, key tile) pairs, B * H_kv * n_t of
+// them, cut into equal runs of per_cta pairs, one run per CTA; seg_max bounds
+// the number of runs that cut one K/V head (1: no head is cut, no combine).
+struct DecodePlan {
+  int n_t, per_cta, grid, seg_max;
+};
+
+static fa_status decode_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int num_ctas,
+                             DecodePlan* p) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || num_ctas < 0) return FA_ERR_INVALID_ARG;
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * Nq >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(H / Hkv) * Nq > fa::kTile) return FA_ERR_UNSUPPORTED;
+  p->n_t = (Nk + fa::kTile - 1) / fa::kTile;
+  const long long total = static_cast<long long>(B) * Hkv * p->n_t;
+  if (total >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  long long ctas = num_ctas;
+  if (ctas == 0) {
+    DeviceInfo* di = nullptr;
+    const fa_status st = device_info(&di);
+    if (st != FA_OK) return st;
+    ctas = di->num_sms;
+  }
+  if (ctas > total) ctas = total;
+  const long long per = (total + ctas - 1) / ctas;
+  p->per_cta = static_cast<int>(per);
+  p->grid = static_cast<int>((total + per - 1) / per);
+  if (per % p->n_t == 0) {
+    p->seg_max = 1;  // every run holds whole heads
+  } else {
+    const int bound = (p->n_t - 1) / p->per_cta + 2;
+    p->seg_max = bound < p->grid ? bound : p->grid;
+  }
+  return FA_OK;
+}
+
+static size_t decode_ws_bytes(int B, int H, int Nq, int d, const DecodePlan& p) {
+  if (p.seg_max <= 1) return 0;
+  const size_t slots = static_cast<size_t>(B) * H * Nq * p.seg_max;
+  return round256(slots * d * sizeof(float)) + round256(slots * sizeof(float));
+}
+
+size_t fa_decode_workspace_size(int B, int H, int H_kv, int Nq, int Nk, int d, int num_ctas) {
+  DecodePlan p;
+  if (decode_plan(B, H, H_kv, Nq, Nk, d, num_ctas, &p) != FA_OK) return 0;
+  return decode_ws_bytes(B, H, Nq, d, p);
+}
+
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
+                    const int32_t* seqlens_k, int num_ctas, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  DecodePlan p;
+  fa_status st = decode_plan(B, H, H_kv, Nq, Nk, d, num_ctas, &p);
+  if (st != FA_OK) return st;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seqlens_k) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  const size_t ws = decode_ws_bytes(B, H, Nq, d, p);
+  if (ws > 0 && (workspace == nullptr || workspace_bytes < ws || !aligned16(workspace)))
+    return FA_ERR_WORKSPACE;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if (!encode_map(&tq, q, 1, B * H * Nq, d) || !encode_map(&tk, k_cache, B * H_kv, Nk, d) ||
+      !encode_map(&tv, v_cache, B * H_kv, Nk, d))
+    return FA_ERR_CUDA;
+  fa::DecodeArgs a;
+  a.B = B;
+  a.H = H;
+  a.Hkv = H_kv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.causal = causal ? 1 : 0;
+  a.seqlens_k = seqlens_k;
+  a.n_t = p.n_t;
+  a.per_cta = p.per_cta;
+  a.seg_max = p.seg_max;
+  a.scale_log2 = scale * fa::kLog2e;
+  a.sync = make_sync(di, false);
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  const size_t slots = static_cast<size_t>(B) * H * Nq * p.seg_max;
+  a.o_part = ws > 0 ? static_cast<float*>(workspace) : nullptr;
+  a.lse_part = ws > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                 round256(slots * d * sizeof(float)))
+                      : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_decode(tq, tk, tv, a, d, p.grid, s);
+  if (e == cudaSuccess && p.seg_max > 1) e = fa::launch_decode_combine(a, d, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_dropout_p8(float dropout_p) { return p8_of(dropout_p); }
 
 fa_status fa_debug_dropout_keep(uint8_t* keep, int B, int H, int N, float dropout_p,

@@ -87,6 +87,51 @@ def draw(w: Workload, with_grad: bool = True):
     return out
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq new query rows per head over a K/V cache of Nk rows (forward only)."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool = False
+    lengths: tuple | None = None  # (lo, hi) inclusive range of valid cache lengths
+    seed: int = 0
+    description: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# Decode: the pages name single-token decode as memory-bound and left
+# unoptimised by the FlashAttention kernels, without a workload; this one is a
+# serving-shaped step of one new token per sequence over a 16K-token cache,
+# grouped K/V heads (4 query heads each), K/V 1.07 GB (well above L2).
+DECODE = DecodeWorkload("decode_16k", 16, 32, 8, 1, 16384, 128,
+                        description="B=16 H=32 H_kv=8 Nq=1 Nk=16384 d=128, one new token per "
+                                    "sequence over a full 16K K/V cache")
+
+
+def draw_decode(w: DecodeWorkload) -> dict:
+    """bf16 CPU tensors q [B,H,Nq,d], k, v [B,Hkv,Nk,d] drawn in that order as
+    randn in fp32, then int32 cache lengths if w.lengths is set, else None."""
+    g = torch.Generator().manual_seed(w.seed)
+    out = {"q": torch.randn((w.B, w.H, w.Nq, w.d), generator=g).to(torch.bfloat16)}
+    for name in ("k", "v"):
+        out[name] = torch.randn((w.B, w.Hkv, w.Nk, w.d), generator=g).to(torch.bfloat16)
+    if w.lengths is not None:
+        lo, hi = w.lengths
+        out["seqlens"] = torch.randint(lo, hi + 1, (w.B,), generator=g,
+                                       dtype=torch.int64).to(torch.int32)
+    else:
+        out["seqlens"] = None
+    return out
+
+
 def draw_small(B, H, N, d, seed=0, with_grad=True, padding=None):
     """Same recipe for an ad-hoc shape (parity cases and edge cases)."""
     w = Workload("adhoc", B, H, N, d, padding=padding, seed=seed)

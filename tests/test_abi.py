@@ -99,3 +99,25 @@ def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(mod, "_lib", None)
     with pytest.raises(RuntimeError):
         mod.load()
+
+
+def test_decode_workspace_size(lib):
+    """Host-side work split of fa_decode, with an explicit CTA count (no device
+    query): B*H_kv*ceil(Nk/128) (K/V head, key tile) pairs in runs of
+    ceil(pairs / CTAs); a run length that is a multiple of the tiles per head
+    cuts no head and needs no workspace; otherwise each query row gets
+    min(runs, (tiles - 1) // run + 2) slots of d + 1 floats (256-byte rounded)."""
+    # 1 x 2 heads x 3 tiles = 6 pairs
+    assert fa.fa_decode_workspace_size(1, 4, 2, 1, 300, 64, 2) == 0       # runs of 3
+    assert fa.fa_decode_workspace_size(1, 4, 2, 1, 300, 64, 1) == 0       # one run of 6
+    # runs of 1: 4 slots x 4 rows: 16 x 64 floats + 16 floats
+    assert fa.fa_decode_workspace_size(1, 4, 2, 1, 300, 64, 6) == 4096 + 256
+    # runs of 2 (3 runs): 3 slots x 4 rows
+    assert fa.fa_decode_workspace_size(1, 4, 2, 1, 300, 64, 4) == 3072 + 256
+    assert fa.fa_decode_workspace_size(1, 4, 2, 1, 300, 64, 1000) == 4096 + 256  # clamped to 6
+    # invalid shapes report 0 (fa_decode itself returns the error)
+    assert fa.fa_decode_workspace_size(1, 3, 2, 1, 300, 64, 4) == 0       # H % H_kv
+    assert fa.fa_decode_workspace_size(1, 4, 1, 64, 300, 64, 4) == 0      # 4 x 64 rows > 128
+    assert fa.fa_decode_workspace_size(1, 4, 2, 1, 300, 96, 4) == 0       # d
+    assert fa.fa_decode_workspace_size(1, 4, 2, 1, 0, 64, 4) == 0         # empty cache dim
+
