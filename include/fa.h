@@ -173,7 +173,9 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  *   (H / H_kv) * Nq <= 128: the query rows of a K/V group form one tile, so
  *   every K/V tile is read from HBM once per group. d = 64 or 128.
  *   num_ctas: number of CTAs the (K/V head, key tile) pairs are divided
- *   among; 0 = one per SM. A K/V head cut between two CTAs is finished by a
+ *   among in equal runs; 0 = automatic: whole K/V heads per CTA when that
+ *   keeps at least 4/5 of the SMs busy, else one CTA per SM with heads cut
+ *   between them. A K/V head cut between two CTAs is finished by a
  *   second, small kernel that merges the pieces' normalised outputs with the
  *   online softmax's merge rule; it needs the caller's workspace of
  *   fa_decode_workspace_size(...) bytes (16-byte aligned, device; 0 when no

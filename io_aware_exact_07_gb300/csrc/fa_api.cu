@@ -394,14 +394,24 @@ static fa_status decode_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int n
   const long long total = static_cast<long long>(B) * Hkv * p->n_t;
   if (total >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   long long ctas = num_ctas;
+  long long per = 0;
   if (ctas == 0) {
     DeviceInfo* di = nullptr;
     const fa_status st = device_info(&di);
     if (st != FA_OK) return st;
     ctas = di->num_sms;
+    // Whole K/V heads per CTA when that still keeps enough SMs streaming to
+    // saturate HBM (measured: 4/5 of them at d = 128, where one CTA streams
+    // about 54 GB/s; all but 1/20 at d = 64, where a CTA is slower than its
+    // share of HBM): no head is cut, so there are no partial results to write
+    // and no combine launch. Otherwise equal runs over all SMs, cutting heads.
+    const long long heads = static_cast<long long>(B) * Hkv;
+    const long long k = (heads + ctas - 1) / ctas;  // heads per CTA
+    const long long busy = (heads + k - 1) / k;      // CTAs that get a head
+    if (d == 128 ? busy * 5 >= ctas * 4 : busy * 20 >= ctas * 19) per = k * p->n_t;
   }
   if (ctas > total) ctas = total;
-  const long long per = (total + ctas - 1) / ctas;
+  if (per == 0) per = (total + ctas - 1) / ctas;
   p->per_cta = static_cast<int>(per);
   p->grid = static_cast<int>((total + per - 1) / per);
   if (per % p->n_t == 0) {

@@ -16,11 +16,14 @@
 //    2; FlashAttention deep-read report, section 2.4).
 //
 // Per CTA: warp 4 is the TMA producer (the Q tile once per piece, K and V
-// tiles through an NS-stage ring), warp 5 issues the tcgen05 MMAs (S = Q K^T
-// into one of two tensor-memory S buffers; O += P V with P read from tensor
-// memory), warps 0-3 run the online softmax with one thread per query row
-// (only the warps that hold real rows take part). Tensor memory: S_0, S_1
-// (128 columns each, P written over S as bf16) and O (d columns).
+// tiles through an NS-stage ring); warp 5 issues S = Q K^T (tcgen05.mma into
+// one of three tensor-memory S buffers) and warp 6 issues O += P V (P read from
+// tensor memory) as soon as the softmax has written P, so that neither kind of
+// MMA waits behind the other's inputs; warps 0-3 run the online softmax with
+// one thread per query row (only the warps that hold real rows take part).
+// Tensor memory: S_0, S_1, S_2 (128 columns each, P written over S as bf16)
+// and O (d columns); three S buffers let the S product of a tile start while
+// the two before it are still in softmax or in their PV product.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -31,11 +34,13 @@ namespace fa {
 
 namespace {
 
-constexpr int kDecThreads = 192;
+constexpr int kDecThreads = 224;
 constexpr int kDecProducerWarp = 4;
-constexpr int kDecMmaWarp = 5;
+constexpr int kDecMmaWarp = 5;  // S issuer; allocates tensor memory
+constexpr int kDecPvWarp = 6;   // PV issuer
 constexpr int kDecMaxStages = 6;
 constexpr float kDecRescale = 8.0f;  // log2 units: rescale O when m grows by > 2^8
+constexpr uint32_t kSBufs = 3;       // S / P buffers in tensor memory
 constexpr int kCombineWarps = 8;
 
 template <int D>
@@ -48,21 +53,22 @@ struct DecL {
   static constexpr int kKOff = kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  // q_full, q_empty, k/v full/empty rings, s_full[2], s_free[2], p_full[2],
-  // pv_done, o_full, o_free, drain
-  static constexpr int kNumBars = 2 + 4 * kDecMaxStages + 10;
+  // q_full, q_empty, k/v full/empty rings, s_full[3], s_free[3], p_full[3],
+  // o_full, o_free, drain, drain_pv
+  static constexpr int kNumBars = 2 + 4 * kDecMaxStages + 3 * kSBufs + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmemBytes <= 232448, "more shared memory than one CTA may hold");
-  static constexpr uint32_t kColO = 256;  // after S_0, S_1
+  static constexpr uint32_t kColO = kSBufs * 128;  // after the S buffers
+  static_assert(kColO + D <= 512, "tensor memory holds the S buffers and O");
 };
 
 struct DecBars {
   uint32_t q_full, q_empty;
   uint32_t k_full[kDecMaxStages], k_empty[kDecMaxStages];
   uint32_t v_full[kDecMaxStages], v_empty[kDecMaxStages];
-  uint32_t s_full[2], s_free[2], p_full[2];
-  uint32_t pv_done, o_full, o_free, drain;
+  uint32_t s_full[kSBufs], s_free[kSBufs], p_full[kSBufs];
+  uint32_t o_full, o_free, drain, drain_pv;
 };
 
 // One piece of a CTA's run: key tiles [j0, j1) of K/V head bkv (j1 already
@@ -135,13 +141,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int s = 0; s < kDecMaxStages; ++s) bars.k_empty[s] = nb();
     for (int s = 0; s < kDecMaxStages; ++s) bars.v_full[s] = nb();
     for (int s = 0; s < kDecMaxStages; ++s) bars.v_empty[s] = nb();
-    for (int x = 0; x < 2; ++x) bars.s_full[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.s_free[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.p_full[x] = nb();
-    bars.pv_done = nb();
+    for (uint32_t x = 0; x < kSBufs; ++x) bars.s_full[x] = nb();
+    for (uint32_t x = 0; x < kSBufs; ++x) bars.s_free[x] = nb();
+    for (uint32_t x = 0; x < kSBufs; ++x) bars.p_full[x] = nb();
     bars.o_full = nb();
     bars.o_free = nb();
     bars.drain = nb();
+    bars.drain_pv = nb();
   }
   if (tid == 0) {
     *abort_flag = 0;
@@ -153,15 +159,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mbar_init(bars.v_full[s], 1);
       mbar_init(bars.v_empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
+    for (uint32_t x = 0; x < kSBufs; ++x) {
       mbar_init(bars.s_full[x], 1);
       mbar_init(bars.s_free[x], 1);
       mbar_init(bars.p_full[x], 32 * n_sw);
     }
-    mbar_init(bars.pv_done, 1);
     mbar_init(bars.o_full, 1);
     mbar_init(bars.o_free, 32 * n_sw);
     mbar_init(bars.drain, 1);
+    mbar_init(bars.drain_pv, 1);
     fence_mbar_init();
   }
   if (warp == kDecMmaWarp) {
@@ -240,18 +246,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     __syncwarp();
   } else if (warp == kDecMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
-      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);   // O += P V, V MN-major
       constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
       const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
       uint32_t it = 0;
       bool ok = true;
       int np = 0;
-      int n_full = 0;  // pieces with at least one key tile so far (O handshakes)
       for (long long pos = lo; pos < hi && ok; ++np) {
         Piece pc;
         pos = make_piece(args, blockIdx.x, pos, hi, pc);
@@ -259,39 +262,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           ok = false;
           break;
         }
-        bool first = true;
-        uint32_t prev_it = 0;
-        int prev_s = 0;
-        // O += P V for the key tile at ring position prev_it (stage prev_s).
-        auto pv = [&]() -> bool {
-          const uint32_t x = prev_it & 1u;
-          if (!mbar_wait(bars.p_full[x], (prev_it >> 1) & 1u, tmo, abort_flag)) return false;
-          if (!mbar_wait(bars.v_full[prev_s], (prev_it / L::kStages) & 1u, tmo, abort_flag))
-            return false;
-          // the epilogue of the previous piece with keys has read O
-          if (first && n_full > 0 && !mbar_wait(bars.o_free, (n_full - 1) & 1, tmo, abort_flag))
-            return false;
-          tc_fence_after();
-          const uint64_t dv = dV0 + static_cast<uint64_t>(prev_s) * kStageStep;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + L::kColO, tmem + x * 128u + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4),
-                   kIdPV, (first && kk == 0) ? 0u : 1u);
-          mma_commit(bars.v_empty[prev_s]);
-          mma_commit(bars.s_free[x]);
-          mma_commit(bars.pv_done);
-          first = false;
-          return true;
-        };
-        for (int j = pc.j0; j < pc.j1 && ok; ++j) {
+        for (int j = pc.j0; j < pc.j1; ++j) {
           const int s = it % L::kStages;
-          const uint32_t x = it & 1u;
+          const uint32_t x = it % kSBufs;
           if (!mbar_wait(bars.k_full[s], (it / L::kStages) & 1u, tmo, abort_flag)) {
             ok = false;
             break;
           }
-          // S buffer x was last read as P by the PV two positions back.
-          if (it >= 2 && !mbar_wait(bars.s_free[x], ((it >> 1) - 1) & 1u, tmo, abort_flag)) {
+          // S buffer x was last read as P by the PV kSBufs positions back.
+          if (it >= kSBufs &&
+              !mbar_wait(bars.s_free[x], ((it / kSBufs) - 1) & 1u, tmo, abort_flag)) {
             ok = false;
             break;
           }
@@ -304,29 +284,61 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
           mma_commit(bars.k_empty[s]);
           mma_commit(bars.s_full[x]);
-          if (j > pc.j0 && !pv()) {
-            ok = false;
-            break;
-          }
-          prev_it = it;
-          prev_s = s;
           ++it;
         }
         if (!ok) break;
-        if (pc.j1 > pc.j0) {
-          if (!pv()) {
-            ok = false;
-            break;
-          }
-          mma_commit(bars.o_full);  // O of this piece is complete once every MMA so far is
-          ++n_full;
-        }
-        mma_commit(bars.q_empty);
+        mma_commit(bars.q_empty);  // Q may be replaced once these S products are done
       }
       if (!ok) fail();
       // Drain: every issued MMA must finish before tensor memory is released.
       mma_commit(bars.drain);
       mbar_wait(bars.drain, 0, tmo, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kDecPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);  // O += P V, V MN-major
+      constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
+      const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
+      uint32_t it = 0;
+      bool ok = true;
+      int n_full = 0;  // pieces with at least one key tile so far (O handshakes)
+      for (long long pos = lo; pos < hi && ok;) {
+        Piece pc;
+        pos = make_piece(args, blockIdx.x, pos, hi, pc);
+        for (int j = pc.j0; j < pc.j1; ++j) {
+          const int s = it % L::kStages;
+          const uint32_t x = it % kSBufs;
+          const bool first = j == pc.j0;
+          if (!mbar_wait(bars.p_full[x], (it / kSBufs) & 1u, tmo, abort_flag) ||
+              !mbar_wait(bars.v_full[s], (it / L::kStages) & 1u, tmo, abort_flag) ||
+              // the epilogue of the previous piece with keys has read O
+              (first && n_full > 0 &&
+               !mbar_wait(bars.o_free, (n_full - 1) & 1, tmo, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + L::kColO, tmem + x * 128u + kk * 8,
+                   dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
+                   (first && kk == 0) ? 0u : 1u);
+          mma_commit(bars.v_empty[s]);
+          mma_commit(bars.s_free[x]);  // also tells the softmax that this PV is done
+          ++it;
+        }
+        if (!ok) break;
+        if (pc.j1 > pc.j0) {
+          mma_commit(bars.o_full);  // O of this piece is complete with its last PV
+          ++n_full;
+        }
+      }
+      if (!ok) fail();
+      mma_commit(bars.drain_pv);
+      mbar_wait(bars.drain_pv, 0, tmo, nullptr);
     }
     __syncwarp();
   } else if (warp < n_sw) {
@@ -353,9 +365,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
       float l_sum = 0.f;        // running sum of exp2(s*c - m_ref)
       for (int j = pc.j0; j < pc.j1; ++j) {
-        const uint32_t x = it & 1u;
+        const uint32_t x = it % kSBufs;
         const uint32_t tS = tmem + lane_base + x * 128u;
-        if (!mbar_wait_warp(bars.s_full[x], (it >> 1) & 1u, tmo, abort_flag)) {
+        if (!mbar_wait_warp(bars.s_full[x], (it / kSBufs) & 1u, tmo, abort_flag)) {
           fail();
           ok = false;
           break;
@@ -392,9 +404,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           l_sum *= alpha;
           m_ref = m_new;
         }
-        // Rescale the O row once the PV of the previous tile has finished with it.
+        // Rescale the O row once the PV of the previous tile has finished with
+        // it (the s_free phase of its buffer; the PV before that on the same
+        // buffer completed before this tile's S was issued).
         if (j > pc.j0 && __any_sync(0xffffffffu, grow)) {
-          if (!mbar_wait_warp(bars.pv_done, (it - 1) & 1u, tmo, abort_flag)) {
+          if (!mbar_wait_warp(bars.s_free[(it - 1) % kSBufs], ((it - 1) / kSBufs) & 1u, tmo,
+                              abort_flag)) {
             fail();
             ok = false;
             break;

@@ -83,17 +83,22 @@ def test_decode_empty_caches():
 
 
 def test_decode_bench_workload_matches_oracle():
-    # The bench's decode step at full size, in the launch configuration it
-    # times (one CTA per SM, heads cut between CTAs), every row checked.
+    # The bench's decode step at full size, every row checked: in the launch
+    # configuration the bench times (automatic split: 128 whole K/V heads on
+    # 128 CTAs) and with one CTA per SM (heads cut, combine kernel).
     w = inputs.DECODE
     x = inputs.draw_decode(w)
-    o, lse = fa.decode(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), w.scale, causal=w.causal)
-    torch.cuda.synchronize()
-    assert fa.fa_decode_workspace_size(w.B, w.H, w.Hkv, w.Nq, w.Nk, w.d, 0) > 0
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
     f64 = lambda t: t.double().numpy()
     o_ref, lse_ref = oracle.fwd_decode(f64(x["q"]), f64(x["k"]), f64(x["v"]), w.scale,
                                        causal=w.causal)
-    check(o, lse, o_ref, lse_ref)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for ctas in (0, sms):
+        o, lse = fa.decode(q, k, v, w.scale, causal=w.causal, num_ctas=ctas)
+        torch.cuda.synchronize()
+        assert fa.fa_device_status() == fa.FA_OK
+        check(o, lse, o_ref, lse_ref)
+    assert fa.fa_decode_workspace_size(w.B, w.H, w.Hkv, w.Nq, w.Nk, w.d, sms) > 0
 
 
 def test_decode_rejects_bad_arguments():
