@@ -652,10 +652,20 @@ def decode_cpu_baseline(w, x, budget_s=12.0):
     t1 = run(groups[:1])
     n = int(max(1, min(len(groups), budget_s / max(t1, 1e-6))))
     t = run(groups[:n]) if n > 1 else t1
-    byts = decode_bytes(w, sl, groups[:n])
-    return {"value": byts / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} of {len(groups)} K/V groups of {w.name} (all their query heads), "
-                      f"fp64 numpy, {t:.1f} s", "seconds": t}
+    reps = 1
+    if n == len(groups) and budget_s > 0:
+        # the whole workload is fast: repeat it so the timing spans a few seconds
+        reps = int(max(1, min(50, 2.0 / max(t, 1e-6))))
+        if reps > 1:
+            t = sum(run(groups) for _ in range(reps))
+    byts = decode_bytes(w, sl, groups[:n]) * reps
+    # numpy's matrix-vector products run in its BLAS, which may use every core
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS",
+                                                                      os.cpu_count() or 1)))
+    return {"value": byts / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {len(groups)} K/V groups of {w.name} (all their query heads)"
+                      f"{f' x{reps}' if reps > 1 else ''}, fp64 numpy (BLAS threads up to "
+                      f"{cores}), {t:.1f} s", "seconds": t}
 
 
 def run_decode_reference(args, w):
@@ -679,7 +689,7 @@ def run_decode_reference(args, w):
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), same inputs)",
         "config": {"workload": w.name, "description": w.description, "bytes_per_step": byts},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
