@@ -7,7 +7,7 @@ never does, and it shares no code with the CUDA sources.
 
 Each function restates a definition from the pages (see ``oracle.c`` for the
 citations): standard attention ("Algorithm 0", FlashAttention deep-read report
-section 3.1) with the fused causal / key-padding / block-sparse masks and
+section 3.1) with the fused causal / key-padding / block-sparse / sliding-window masks and
 dropout of section 3.2, its analytic backward, Philox4x32-10 (Salmon et al.,
 SC'11) and the butterfly block mask of sections 2.6 / 3.5.
 
@@ -68,7 +68,8 @@ def _load():
                                             ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64]
         lib.oracle_dropout_keep.restype = None
         common = [ctypes.c_int, ip, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                  ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, u8, ip]
+                  ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, u8, ip,
+                  ctypes.c_int, ctypes.c_int]
         lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp] + common
         lib.oracle_fwd.restype = ctypes.c_int
         lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp] + common
@@ -134,8 +135,11 @@ def _opt(block_mask, seqlens_k):
 
 
 def fwd(q, k, v, scale, causal=False, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        seqlens_k=None, heads=None, H=None):
+        seqlens_k=None, heads=None, H=None, window_left=-1, window_right=-1):
     """Standard attention forward in fp64.
+
+    window_left / window_right: sliding window, key j visible to query i only
+    if i - window_left <= j <= i + window_right (-1: that side unbounded).
 
     q, k, v: [n, N, d] arrays (one entry per head listed in ``heads``, a list
     of (b, h) pairs; default: all heads of a [B, H, N, d] tensor, in which
@@ -160,7 +164,8 @@ def fwd(q, k, v, scale, causal=False, dropout_p=0.0, seed=0, offset=0, block_mas
                             _ptr(v, ctypes.c_double), _ptr(o, ctypes.c_double),
                             _ptr(lse, ctypes.c_double), n, _ptr(hb, ctypes.c_int),
                             _ptr(hh, ctypes.c_int), int(H), N, d, float(scale), int(bool(causal)),
-                            p8(dropout_p), int(seed), int(offset), bmp, slp)
+                            p8(dropout_p), int(seed), int(offset), bmp, slp, int(window_left),
+                            int(window_right))
     if rc != 0:
         raise RuntimeError(f"oracle_fwd failed: {rc}")
     if shape4 is not None:
@@ -170,7 +175,7 @@ def fwd(q, k, v, scale, causal=False, dropout_p=0.0, seed=0, offset=0, block_mas
 
 
 def bwd(q, k, v, dout, scale, causal=False, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        seqlens_k=None, heads=None, H=None):
+        seqlens_k=None, heads=None, H=None, window_left=-1, window_right=-1):
     """Analytic backward of L = sum(O * dO) in fp64. Returns (dq, dk, dv, D)."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     shape4 = None
@@ -195,7 +200,7 @@ def bwd(q, k, v, dout, scale, causal=False, dropout_p=0.0, seed=0, offset=0, blo
                             _ptr(dv, ctypes.c_double), _ptr(D, ctypes.c_double), n,
                             _ptr(hb, ctypes.c_int), _ptr(hh, ctypes.c_int), int(H), N, d,
                             float(scale), int(bool(causal)), p8(dropout_p), int(seed),
-                            int(offset), bmp, slp)
+                            int(offset), bmp, slp, int(window_left), int(window_right))
     if rc != 0:
         raise RuntimeError(f"oracle_bwd failed: {rc}")
     if shape4 is not None:

@@ -16,6 +16,15 @@
  *   and dropout done on chip) are applied as plain element-wise steps:
  *
  *     allowed(i,j) = [!causal || j <= i] && [j < L_b] && [block_mask[i/128][j/128]]
+ *                    && [wl < 0 || j >= i - wl] && [wr < 0 || j <= i + wr]
+ *
+ *   The last two factors are the sliding (local) window: a key is visible to a
+ *   query only within wl positions before it and wr after it (a negative value
+ *   leaves that side unbounded). The cross-paper synthesis page on
+ *   FlashAttention lists sliding-window attention among the variants an
+ *   IO-aware kernel should cover (section 5), and the Attention Kernel page
+ *   counts sliding windows among the sparse patterns whose blocks are skipped
+ *   (its section on xFormers, cuDNN and sparse attention).
  *     s_ij   = scale * q_i . k_j                          (allowed pairs only)
  *     lse_i  = m_i + ln sum_j exp(s_ij - m_i),   m_i = max_j s_ij
  *     P_ij   = exp(s_ij - lse_i)                          (0 where not allowed)
@@ -146,6 +155,7 @@ void oracle_butterfly(uint8_t* mask, int nb) {
 
 typedef struct {
   int H, N, d, causal, p8;
+  int wl, wr;  /* sliding window: keys i - wl .. i + wr (negative: unbounded) */
   double scale, keep_scale;
   uint64_t seed, offset;
   const uint8_t* block_mask;
@@ -154,8 +164,11 @@ typedef struct {
 } params_t;
 
 static params_t make_params(int H, int N, int d, double scale, int causal, int p8, uint64_t seed,
-                            uint64_t offset, const uint8_t* block_mask, const int* seqlens_k) {
+                            uint64_t offset, const uint8_t* block_mask, const int* seqlens_k,
+                            int wl, int wr) {
   params_t P;
+  P.wl = wl;
+  P.wr = wr;
   P.H = H;
   P.N = N;
   P.d = d;
@@ -173,6 +186,8 @@ static params_t make_params(int H, int N, int d, double scale, int causal, int p
 
 static int allowed(const params_t* P, int b, int i, int j) {
   if (P->causal && j > i) return 0;
+  if (P->wl >= 0 && j < i - P->wl) return 0;
+  if (P->wr >= 0 && j > i + P->wr) return 0;
   if (P->seqlens_k && j >= P->seqlens_k[b]) return 0;
   if (P->block_mask && !P->block_mask[(long)(i / ORACLE_BLOCK) * P->nb + (j / ORACLE_BLOCK)])
     return 0;
@@ -206,9 +221,11 @@ static double row_lse(const params_t* P, int b, int i, const double* qi, const d
 int oracle_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
                int n_heads, const int* head_b, const int* head_h, int H, int N, int d,
                double scale, int causal, int p8, uint64_t seed, uint64_t offset,
-               const uint8_t* block_mask, const int* seqlens_k) {
+               const uint8_t* block_mask, const int* seqlens_k, int window_left,
+               int window_right) {
   if (n_heads < 0 || N < 0 || d <= 0) return 1;
-  params_t P = make_params(H, N, d, scale, causal, p8, seed, offset, block_mask, seqlens_k);
+  params_t P = make_params(H, N, d, scale, causal, p8, seed, offset, block_mask, seqlens_k,
+                           window_left, window_right);
   long total = (long)n_heads * N;
 #pragma omp parallel
   {
@@ -244,9 +261,11 @@ int oracle_fwd(const double* q, const double* k, const double* v, double* o, dou
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dout, double* dq,
                double* dk, double* dv, double* D, int n_heads, const int* head_b,
                const int* head_h, int H, int N, int d, double scale, int causal, int p8,
-               uint64_t seed, uint64_t offset, const uint8_t* block_mask, const int* seqlens_k) {
+               uint64_t seed, uint64_t offset, const uint8_t* block_mask, const int* seqlens_k,
+               int window_left, int window_right) {
   if (n_heads < 0 || N < 0 || d <= 0) return 1;
-  params_t P = make_params(H, N, d, scale, causal, p8, seed, offset, block_mask, seqlens_k);
+  params_t P = make_params(H, N, d, scale, causal, p8, seed, offset, block_mask, seqlens_k,
+                           window_left, window_right);
   long total = (long)n_heads * N;
   double* lse = (double*)malloc(sizeof(double) * (total > 0 ? total : 1));
   if (!lse) return 2;
