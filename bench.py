@@ -61,13 +61,16 @@ def allowed_pairs(w: inputs.Workload, seqlens) -> int:
         mask = (x == 0) | ((x & (x - 1)) == 0)
     lens = [N] * w.B if seqlens is None else [min(max(int(s), 0), N) for s in seqlens]
     rows = np.arange(N)
+    wl, wr = w.window
+    # per row, the visible keys form [lo, hi) before the block mask
+    lo_r = np.zeros(N, dtype=np.int64) if wl < 0 else np.maximum(rows - wl, 0)
+    hi_r = rows + 1 if w.causal else np.full(N, N, dtype=np.int64)
+    if wr >= 0:
+        hi_r = np.minimum(hi_r, rows + wr + 1)
     total = 0
     for L in lens:
-        if not w.causal and mask is None:
-            total += N * L
-            continue
-        if mask is None:  # causal, possibly padded: keys j <= i and j < L
-            total += int(np.minimum(rows + 1, L).sum())
+        if mask is None:  # dense, causal, padded and / or windowed
+            total += int(np.clip(np.minimum(hi_r, L) - lo_r, 0, None).sum())
             continue
         cnt = 0
         for qt in range(nb):
@@ -78,8 +81,9 @@ def allowed_pairs(w: inputs.Workload, seqlens) -> int:
                 lo, hi = kt * T, min((kt + 1) * T, L)
                 if hi <= lo:
                     continue
-                hi_r = np.minimum(hi, r + 1) if w.causal else np.full_like(r, hi)
-                cnt += int(np.clip(hi_r - lo, 0, None).sum())
+                hi_t = np.minimum(hi, hi_r[qt * T:(qt + 1) * T])
+                lo_t = np.maximum(lo, lo_r[qt * T:(qt + 1) * T])
+                cnt += int(np.clip(hi_t - lo_t, 0, None).sum())
         total += cnt
     return total * w.H
 
@@ -185,10 +189,11 @@ class Step:
         if w.butterfly:
             self.bm = fa.fa_butterfly_mask(math.ceil(w.N / 128)).to(dev)
         B, H, N, d = w.B, w.H, w.N, w.d
-        # grouped K/V heads go through fa_fwd_gqa / fa_bwd_gqa, timed as fwd and
-        # the whole backward (the per-stage entry points are per-head only)
-        self.gqa = w.kv_heads != H
-        self.kernels = ("fwd", "bwd") if self.gqa else KERNELS
+        # grouped K/V heads and sliding windows go through fa_fwd_window /
+        # fa_bwd_window, timed as fwd and the whole backward (the per-stage
+        # entry points take neither)
+        self.whole = w.kv_heads != H or tuple(w.window) != (-1, -1)
+        self.kernels = ("fwd", "bwd") if self.whole else KERNELS
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         self.dq = torch.empty_like(self.q)
@@ -203,16 +208,18 @@ class Step:
         B, H, N, d, s = w.B, w.H, w.N, w.d, w.scale
         o = self.opts
         ev = events or [None] * 5
-        if self.gqa:
+        if self.whole:
             Hkv = w.kv_heads
+            win = dict(window_left=w.window[0], window_right=w.window[1])
             if ev[0] is not None:
                 ev[0].record()
-            st = fa.fa_fwd_gqa(self.q, self.k, self.v, self.o, self.lse, B, H, Hkv, N, d, s, **o)
+            st = fa.fa_fwd_window(self.q, self.k, self.v, self.o, self.lse, B, H, Hkv, N, d, s,
+                                  **win, **o)
             if ev[1] is not None:
                 ev[1].record()
-            st |= fa.fa_bwd_gqa(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq,
-                                self.dk, self.dv, B, H, Hkv, N, d, s, workspace=self.ws,
-                                workspace_bytes=self.ws_bytes, **o)
+            st |= fa.fa_bwd_window(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq,
+                                   self.dk, self.dv, B, H, Hkv, N, d, s, workspace=self.ws,
+                                   workspace_bytes=self.ws_bytes, **win, **o)
             if ev[2] is not None:
                 ev[2].record()
             if st != 0:
@@ -290,7 +297,8 @@ def cpu_baseline(w, x, seqlens, budget_s=15.0):
         k, v = f64kv(x["k"]), f64kv(x["v"])
         t0 = time.perf_counter()
         kw = dict(causal=w.causal, dropout_p=w.dropout_p, seed=0, offset=0, block_mask=bm,
-                  seqlens_k=sl_np, heads=heads, H=w.H)
+                  seqlens_k=sl_np, heads=heads, H=w.H, window_left=w.window[0],
+                  window_right=w.window[1])
         oracle.fwd(q, k, v, w.scale, **kw)
         oracle.bwd(q, k, v, do, w.scale, **kw)
         return time.perf_counter() - t0
@@ -305,7 +313,8 @@ def cpu_baseline(w, x, seqlens, budget_s=15.0):
         per_b[b] = per_b.get(b, 0) + 1
     pairs = 0
     for b, cnt in per_b.items():
-        wb = inputs.Workload("s", 1, cnt, w.N, w.d, causal=w.causal, butterfly=w.butterfly)
+        wb = inputs.Workload("s", 1, cnt, w.N, w.d, causal=w.causal, butterfly=w.butterfly,
+                             window=w.window)
         pairs += allowed_pairs(wb, None if seqlens is None else [int(seqlens[b])])
     flops = 14.0 * w.d * pairs
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
@@ -427,7 +436,7 @@ def run_ours(args, w):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; no dataset)",
         "config": {"workload": w.name, "description": w.description, "B": w.B, "H": w.H,
-                   "H_kv": w.kv_heads,
+                   "H_kv": w.kv_heads, "window": list(w.window),
                    "N": w.N, "d": w.d, "causal": w.causal, "dropout_p": w.dropout_p,
                    "key_padding": w.padding, "block_mask": "butterfly" if w.butterfly else None,
                    "allowed_pairs": pairs, "flops_per_step": flops_step,
@@ -474,8 +483,10 @@ def run_reference(args, w):
     f64 = lambda t: np.stack([t[b, h].double().numpy() for b, h in heads])
     q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))  # head 0 uses K/V head 0
     kw = dict(causal=w.causal, dropout_p=w.dropout_p, seed=0, offset=0, block_mask=bm,
-              seqlens_k=sl_np, heads=heads, H=w.H)
-    wb = inputs.Workload("s", 1, 1, w.N, w.d, causal=w.causal, butterfly=w.butterfly)
+              seqlens_k=sl_np, heads=heads, H=w.H, window_left=w.window[0],
+              window_right=w.window[1])
+    wb = inputs.Workload("s", 1, 1, w.N, w.d, causal=w.causal, butterfly=w.butterfly,
+                         window=w.window)
     pairs = allowed_pairs(wb, None if seqlens is None else [int(seqlens[0])])
     flops = 14.0 * w.d * pairs
 

@@ -113,6 +113,29 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                      uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Sliding-window (local) attention, with every other option of fa_fwd_gqa /
+ * fa_bwd_gqa: key j is visible to query i only if
+ * i - window_left <= j <= i + window_right (-1 leaves that side unbounded);
+ * it composes with causal (which caps j <= i), key padding and the block mask.
+ * The cross-paper synthesis page on FlashAttention lists sliding-window
+ * attention among the variants an IO-aware kernel should cover (section 5),
+ * and the Attention Kernel page counts sliding windows among the sparse
+ * patterns whose blocks are skipped (section on xFormers, cuDNN and sparse
+ * attention). The kernels skip every 128 x 128 tile the band misses and mask
+ * elements only on tiles an edge crosses, so the work is O(N * window).
+ * Arguments, layouts, outputs and errors are those of fa_fwd_gqa /
+ * fa_bwd_gqa, plus FA_ERR_INVALID_ARG when a window bound is below -1. */
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+                        int window_right, float dropout_p, uint64_t seed, uint64_t offset,
+                        const uint8_t* block_mask, const int32_t* seqlens_k, void* stream);
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+                        int window_right, float dropout_p, uint64_t seed, uint64_t offset,
+                        const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* The three stages fa_bwd runs, for callers that schedule or time them
  * separately. They must run in this order on one stream with the same
  * workspace (it carries D from the first stage to the other two); dK/dV and

@@ -32,7 +32,8 @@ FA_ERR_TIMEOUT = 5
 
 # Symbols declared in include/fa.h.
 EXPORTS = (
-    "fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_workspace_size", "fa_bwd_preprocess",
+    "fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_window", "fa_bwd_window",
+    "fa_bwd_workspace_size", "fa_bwd_preprocess",
     "fa_bwd_dkdv", "fa_bwd_dq", "fa_decode", "fa_decode_workspace_size",
     "fa_bwd_noalloc", "fa_dropout_p8", "fa_debug_dropout_keep",
     "fa_debug_philox", "fa_butterfly_mask", "fa_device_status", "fa_set_wait_timeout_ns",
@@ -78,6 +79,12 @@ def load(build_if_missing: bool = False):
         lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, f, u64,
                                    u64, vp, vp, vp, sz, vp]
         lib.fa_bwd_gqa.restype = i
+        lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, f, u64, u64,
+                                      vp, vp, vp]
+        lib.fa_fwd_window.restype = i
+        lib.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i,
+                                      f, u64, u64, vp, vp, vp, sz, vp]
+        lib.fa_bwd_window.restype = i
         lib.fa_bwd_preprocess.argtypes = [vp, vp, i, i, i, i, vp, sz, vp]
         lib.fa_bwd_preprocess.restype = i
         lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, f, u64, u64, vp,
@@ -204,6 +211,28 @@ def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causa
                              _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
+def fa_fwd_window(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal=False, window_left=-1,
+                  window_right=-1, dropout_p=0.0, seed=0, offset=0, block_mask=None,
+                  seqlens_k=None, stream=None) -> int:
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N, d,
+                                float(scale), int(bool(causal)), int(window_left),
+                                int(window_right), float(dropout_p), int(seed), int(offset), bm,
+                                sl, _stream(stream))
+
+
+def fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal=False,
+                  window_left=-1, window_right=-1, dropout_p=0.0, seed=0, offset=0,
+                  block_mask=None, seqlens_k=None, workspace=None, workspace_bytes=0,
+                  stream=None) -> int:
+    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    return load().fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, H_kv, N, d, float(scale),
+                                int(bool(causal)), int(window_left), int(window_right),
+                                float(dropout_p), int(seed), int(offset), bm, sl, _ptr(workspace),
+                                int(workspace_bytes), _stream(stream))
+
+
 def fa_bwd_preprocess(o, dout, B, H, N, d, workspace, workspace_bytes, stream=None) -> int:
     return load().fa_bwd_preprocess(_ptr(o), _ptr(dout), B, H, N, d, _ptr(workspace),
                                     int(workspace_bytes), _stream(stream))
@@ -291,9 +320,10 @@ def fa_test_inject_stall(mode: int) -> None:
 # ----------------------------------------------------------- conveniences
 
 def fwd(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0, block_mask=None,
-        seqlens_k=None, stream=None):
+        seqlens_k=None, stream=None, window=(-1, -1)):
     """Allocate O and lse with torch and run fa_fwd (fa_fwd_gqa when k and v
-    have fewer heads than q). Returns (o, lse)."""
+    have fewer heads than q, fa_fwd_window when window = (left, right) is
+    set). Returns (o, lse)."""
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
     Hkv = _kv_heads(q, k, v)
@@ -301,7 +331,10 @@ def fwd(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0, bloc
         scale = 1.0 / math.sqrt(d)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if Hkv == H:
+    if tuple(window) != (-1, -1):
+        st = fa_fwd_window(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, window[0], window[1],
+                           dropout_p, seed, offset, block_mask, seqlens_k, stream)
+    elif Hkv == H:
         st = fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dropout_p, seed, offset,
                     block_mask, seqlens_k, stream)
     else:
@@ -312,9 +345,10 @@ def fwd(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0, bloc
 
 
 def bwd(q, k, v, o, dout, lse, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0,
-        block_mask=None, seqlens_k=None, workspace=None, stream=None):
+        block_mask=None, seqlens_k=None, workspace=None, stream=None, window=(-1, -1)):
     """Allocate dQ, dK, dV (and the workspace if not given) and run fa_bwd
-    (fa_bwd_gqa when k and v have fewer heads than q)."""
+    (fa_bwd_gqa when k and v have fewer heads than q, fa_bwd_window when
+    window = (left, right) is set)."""
     _check_qkv(q, k, v, o, dout)
     B, H, N, d = q.shape
     Hkv = _kv_heads(q, k, v)
@@ -324,7 +358,11 @@ def bwd(q, k, v, o, dout, lse, scale=None, causal=False, dropout_p=0.0, seed=0, 
     ws_bytes = fa_bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    if Hkv == H:
+    if tuple(window) != (-1, -1):
+        st = fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal,
+                           window[0], window[1], dropout_p, seed, offset, block_mask, seqlens_k,
+                           workspace, workspace.numel(), stream)
+    elif Hkv == H:
         st = fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, dropout_p, seed,
                     offset, block_mask, seqlens_k, workspace, workspace.numel(), stream)
     else:

@@ -109,7 +109,7 @@ bool encode_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
 }
 
 fa::MaskParams make_mask(int B, int H, int Hkv, int N, int causal, const uint8_t* bm,
-                         const int32_t* sl) {
+                         const int32_t* sl, int wl = -1, int wr = -1) {
   fa::MaskParams m;
   m.B = B;
   m.H = H;
@@ -117,6 +117,8 @@ fa::MaskParams make_mask(int B, int H, int Hkv, int N, int causal, const uint8_t
   m.N = N;
   m.nb = (N + fa::kTile - 1) / fa::kTile;
   m.causal = causal ? 1 : 0;
+  m.wl = wl;
+  m.wr = wr;
   m.block_mask = bm;
   m.seqlens_k = sl;
   return m;
@@ -164,11 +166,12 @@ std::mutex g_noalloc_mutex;
 extern "C" {
 
 static fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                          int H, int Hkv, int N, int d, float scale, int causal, float dropout_p,
-                          uint64_t seed, uint64_t offset, const uint8_t* block_mask,
-                          const int32_t* seqlens_k, void* stream) {
+                          int H, int Hkv, int N, int d, float scale, int causal, int wl, int wr,
+                          float dropout_p, uint64_t seed, uint64_t offset,
+                          const uint8_t* block_mask, const int32_t* seqlens_k, void* stream) {
   fa_status st = check_common(B, H, N, d, scale, dropout_p, Hkv);
   if (st != FA_OK) return st;
+  if (wl < -1 || wr < -1) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
@@ -179,7 +182,7 @@ static fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, 
       !encode_map(&tv, v, B * Hkv, N, d))
     return FA_ERR_CUDA;
   fa::FwdArgs a;
-  a.mask = make_mask(B, H, Hkv, N, causal, block_mask, seqlens_k);
+  a.mask = make_mask(B, H, Hkv, N, causal, block_mask, seqlens_k, wl, wr);
   a.drop = make_drop(dropout_p, seed, offset);
   a.sync = make_sync(di, true);
   a.scale_log2 = scale * fa::kLog2e;
@@ -194,7 +197,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int N, int d, float scale, int causal, float dropout_p, uint64_t seed,
                  uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
                  void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, H, N, d, scale, causal, dropout_p, seed, offset,
+  return fwd_impl(q, k, v, o, lse, B, H, H, N, d, scale, causal, -1, -1, dropout_p, seed, offset,
                   block_mask, seqlens_k, stream);
 }
 
@@ -202,8 +205,16 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
                      int H, int H_kv, int N, int d, float scale, int causal, float dropout_p,
                      uint64_t seed, uint64_t offset, const uint8_t* block_mask,
                      const int32_t* seqlens_k, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, dropout_p, seed, offset,
-                  block_mask, seqlens_k, stream);
+  return fwd_impl(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, -1, -1, dropout_p, seed,
+                  offset, block_mask, seqlens_k, stream);
+}
+
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+                        int window_right, float dropout_p, uint64_t seed, uint64_t offset,
+                        const uint8_t* block_mask, const int32_t* seqlens_k, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window_left, window_right,
+                  dropout_p, seed, offset, block_mask, seqlens_k, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -217,12 +228,13 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 static fa_status bwd_prepare(const void* q, const void* k, const void* v, const void* o,
                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
                              int B, int H, int Hkv, int N, int d, float scale, int causal,
-                             float dropout_p, uint64_t seed, uint64_t offset,
+                             int wl, int wr, float dropout_p, uint64_t seed, uint64_t offset,
                              const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
                              size_t workspace_bytes, int need, fa::BwdArgs* a, CUtensorMap* maps,
                              DeviceInfo** di) {
   fa_status st = check_common(B, H, N, d, scale, dropout_p, Hkv);
   if (st != FA_OK) return st;
+  if (wl < -1 || wr < -1) return FA_ERR_INVALID_ARG;
   if (need & 1) {
     if (!o || !dout || !aligned16(o) || !aligned16(dout)) return FA_ERR_INVALID_ARG;
   }
@@ -243,7 +255,7 @@ static fa_status bwd_prepare(const void* q, const void* k, const void* v, const 
         !encode_map(&maps[2], v, B * Hkv, N, d) || !encode_map(&maps[3], dout, B * H, N, d))
       return FA_ERR_CUDA;
   }
-  a->mask = make_mask(B, H, Hkv, N, causal, block_mask, seqlens_k);
+  a->mask = make_mask(B, H, Hkv, N, causal, block_mask, seqlens_k, wl, wr);
   a->drop = make_drop(dropout_p, seed, offset);
   a->sync = make_sync(*di, false);
   a->scale = scale;
@@ -260,15 +272,15 @@ static fa_status bwd_prepare(const void* q, const void* k, const void* v, const 
 
 static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
                           const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
-                          int H, int Hkv, int N, int d, float scale, int causal, float dropout_p,
-                          uint64_t seed, uint64_t offset, const uint8_t* block_mask,
-                          const int32_t* seqlens_k, void* workspace, size_t workspace_bytes,
-                          void* stream) {
+                          int H, int Hkv, int N, int d, float scale, int causal, int wl, int wr,
+                          float dropout_p, uint64_t seed, uint64_t offset,
+                          const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                          size_t workspace_bytes, void* stream) {
   fa::BwdArgs a;
   CUtensorMap m[4];
   DeviceInfo* di = nullptr;
   fa_status st = bwd_prepare(q, k, v, o, dout, lse, dq, dk, dv, B, H, Hkv, N, d, scale, causal,
-                             dropout_p, seed, offset, block_mask, seqlens_k, workspace,
+                             wl, wr, dropout_p, seed, offset, block_mask, seqlens_k, workspace,
                              workspace_bytes, 7, &a, m, &di);
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -284,8 +296,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, float dropout_p, uint64_t seed, uint64_t offset,
                  const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
                  size_t workspace_bytes, void* stream) {
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, N, d, scale, causal, dropout_p, seed,
-                  offset, block_mask, seqlens_k, workspace, workspace_bytes, stream);
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, N, d, scale, causal, -1, -1,
+                  dropout_p, seed, offset, block_mask, seqlens_k, workspace, workspace_bytes,
+                  stream);
 }
 
 fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -293,8 +306,20 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                      int d, float scale, int causal, float dropout_p, uint64_t seed,
                      uint64_t offset, const uint8_t* block_mask, const int32_t* seqlens_k,
                      void* workspace, size_t workspace_bytes, void* stream) {
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal, dropout_p,
-                  seed, offset, block_mask, seqlens_k, workspace, workspace_bytes, stream);
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal, -1, -1,
+                  dropout_p, seed, offset, block_mask, seqlens_k, workspace, workspace_bytes,
+                  stream);
+}
+
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+                        int window_right, float dropout_p, uint64_t seed, uint64_t offset,
+                        const uint8_t* block_mask, const int32_t* seqlens_k, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal, window_left,
+                  window_right, dropout_p, seed, offset, block_mask, seqlens_k, workspace,
+                  workspace_bytes, stream);
 }
 
 fa_status fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int N, int d,
@@ -303,8 +328,8 @@ fa_status fa_bwd_preprocess(const void* o, const void* dout, int B, int H, int N
   CUtensorMap m[4];
   DeviceInfo* di = nullptr;
   fa_status st = bwd_prepare(nullptr, nullptr, nullptr, o, dout, nullptr, nullptr, nullptr,
-                             nullptr, B, H, H, N, d, 1.f, 0, 0.f, 0, 0, nullptr, nullptr, workspace,
-                             workspace_bytes, 1, &a, m, &di);
+                             nullptr, B, H, H, N, d, 1.f, 0, -1, -1, 0.f, 0, 0, nullptr, nullptr,
+                             workspace, workspace_bytes, 1, &a, m, &di);
   if (st != FA_OK) return st;
   return fa::launch_bwd_preprocess(a, d, di->num_sms, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
@@ -321,8 +346,8 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
   CUtensorMap m[4];
   DeviceInfo* di = nullptr;
   fa_status st = bwd_prepare(q, k, v, nullptr, dout, lse, nullptr, dk, dv, B, H, H, N, d, scale,
-                             causal, dropout_p, seed, offset, block_mask, seqlens_k, workspace,
-                             workspace_bytes, 2, &a, m, &di);
+                             causal, -1, -1, dropout_p, seed, offset, block_mask, seqlens_k,
+                             workspace, workspace_bytes, 2, &a, m, &di);
   if (st != FA_OK) return st;
   return fa::launch_bwd_dkdv(m[0], m[1], m[2], m[3], a, d, a.drop.p8 > 0, di->num_sms,
                              static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -339,8 +364,8 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dou
   CUtensorMap m[4];
   DeviceInfo* di = nullptr;
   fa_status st = bwd_prepare(q, k, v, nullptr, dout, lse, dq, nullptr, nullptr, B, H, H, N, d,
-                             scale, causal, dropout_p, seed, offset, block_mask, seqlens_k,
-                             workspace, workspace_bytes, 4, &a, m, &di);
+                             scale, causal, -1, -1, dropout_p, seed, offset, block_mask,
+                             seqlens_k, workspace, workspace_bytes, 4, &a, m, &di);
   if (st != FA_OK) return st;
   return fa::launch_bwd_dq(m[0], m[1], m[2], m[3], a, d, a.drop.p8 > 0, di->num_sms,
                            static_cast<cudaStream_t>(stream)) == cudaSuccess

@@ -104,7 +104,7 @@ struct DkdvLayout {
   __device__ static constexpr uint32_t col_dpt() { return static_cast<uint32_t>(2 * D + 128); }
 };
 
-template <int D, bool DROPOUT, bool GQA>
+template <int D, bool DROPOUT, bool GQA, bool WIN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
              ++bh) {  // the query heads sharing this K/V head
         for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           while (bits != 0u) {
             const int qt = chunk * 32 + (__ffs(bits) - 1);
             bits &= bits - 1;
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
              ++bh) {  // the query heads sharing this K/V head
         for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           while (bits != 0u) {
             bits &= bits - 1;
             const int s = it % L::kStages;
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
              ++bh) {  // the query heads sharing this K/V head
         for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           while (bits != 0u) {
             const int qt = chunk * 32 + (__ffs(bits) - 1);
             bits &= bits - 1;
@@ -469,11 +469,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
               }
             }
-            if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
+            if (tile_needs_element_mask<WIN>(mk, qt, kt, kv_len)) {
               const bool key_ok = key < kv_len;
   #pragma unroll
               for (int c = 0; c < 64; ++c) {
-                const bool allowed = key_ok && (!mk.causal || key <= q0 + c);
+                const bool allowed = key_ok && (!mk.causal || key <= q0 + c) &&
+                                     (!WIN || in_window(mk, q0 + c, key));
                 p[c] = allowed ? p[c] : 0.f;
               }
             }
@@ -613,8 +614,11 @@ template <int D, bool DROP>
 static cudaError_t launch_dkdv_impl(const CUtensorMap& tq, const CUtensorMap& tk,
                                     const CUtensorMap& tv, const CUtensorMap& tdo,
                                     const BwdArgs& a, int grid, cudaStream_t stream) {
-  auto kern = a.mask.Hkv != a.mask.H ? fa_bwd_dkdv_kernel<D, DROP, true>
-                                     : fa_bwd_dkdv_kernel<D, DROP, false>;
+  const bool gqa = a.mask.Hkv != a.mask.H, win = a.mask.wl >= 0 || a.mask.wr >= 0;
+  auto kern = gqa ? (win ? fa_bwd_dkdv_kernel<D, DROP, true, true>
+                         : fa_bwd_dkdv_kernel<D, DROP, true, false>)
+                  : (win ? fa_bwd_dkdv_kernel<D, DROP, false, true>
+                         : fa_bwd_dkdv_kernel<D, DROP, false, false>);
   cudaError_t e = set_smem(kern, DkdvLayout<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, kBwdThreads, DkdvLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);

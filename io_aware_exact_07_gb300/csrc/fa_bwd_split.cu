@@ -18,6 +18,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "fa_common.cuh"
 #include "fa_kernels.h"
 
@@ -112,7 +114,7 @@ struct DkdvBars {
   uint32_t acc_full, acc_free, drain_a, drain_b;
 };
 
-template <int D, bool DROPOUT, bool GQA>
+template <int D, bool DROPOUT, bool GQA, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_split_kernel(const __grid_constant__ CUtensorMap tm_q,
                              const __grid_constant__ CUtensorMap tm_k,
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
              ++bh) {  // the query heads sharing this K/V head
         for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           while (bits != 0u) {
             const int qt = chunk * 32 + (__ffs(bits) - 1);
             bits &= bits - 1;
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
              ++bh) {  // the query heads sharing this K/V head
         for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          const uint32_t vbits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          const uint32_t vbits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           if (leader) {
             for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
               const int s = it % L::kStages;
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
              ++bh) {  // the query heads sharing this K/V head
         for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          const uint32_t vbits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          const uint32_t vbits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           if (leader) {
             for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
               const int s = it % L::kStages;
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
              ++bh) {  // the query heads sharing this K/V head
         for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          uint32_t bits = warp_valid_bits_t(mk, kt, chunk, n_t, n_kv);
+          uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           while (bits != 0u && ok) {
             const int qt = chunk * 32 + (__ffs(bits) - 1);
             bits &= bits - 1;
@@ -491,11 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
-            if (tile_needs_element_mask(mk, qt, kt, kv_len)) {
+            if (tile_needs_element_mask<WIN>(mk, qt, kt, kv_len)) {
               const bool key_ok = key < kv_len;
   #pragma unroll
               for (int c = 0; c < 32; ++c)
-                p[c] = (key_ok && (!mk.causal || key <= q0 + c)) ? p[c] : 0.f;
+                p[c] = (key_ok && (!mk.causal || key <= q0 + c) &&
+                        (!WIN || in_window(mk, q0 + c, key)))
+                           ? p[c]
+                           : 0.f;
             }
             {
               uint32_t pk[16];  // dropped copy for dV
@@ -656,7 +661,7 @@ struct DqBars {
   uint32_t drain_a, drain_b;
 };
 
-template <int D, bool DROPOUT>
+template <int D, bool DROPOUT, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_split_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
@@ -779,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++qd_arms[qb];
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits(mk, qt, chunk, n_q, n_kv);
+        uint32_t bits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
         while (bits != 0u) {
           const int j = chunk * 32 + (__ffs(bits) - 1);
           bits &= bits - 1;
@@ -840,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ = sdesc_sw128(sQD + (2 * qb) * T, 16, 1024);
       const uint64_t dDO = sdesc_sw128(sQD + (2 * qb + 1) * T, 16, 1024);
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        const uint32_t vbits = warp_valid_bits(mk, qt, chunk, n_q, n_kv);
+        const uint32_t vbits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
         if (leader) {
           for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
             const int ks = it % L::kKStages, vs = it % L::kVStages;
@@ -889,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int jmax = kv_limit(qt, n_kv);
       bool first = true;
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        const uint32_t vbits = warp_valid_bits(mk, qt, chunk, n_q, n_kv);
+        const uint32_t vbits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
         if (leader) {
           for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
             const int ks = it % L::kKStages;
@@ -965,9 +970,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kv_len = kv_len_of(mk, bh / mk.H);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       const int jmax = kv_limit(qt, n_kv);
+      // sliding window: keys [key_lo, key_hi) are visible to this row
+      int key_lo = 0, key_hi = kv_len;
+      if constexpr (WIN) {
+        if (mk.causal && row + 1 < key_hi) key_hi = row + 1;
+        if (mk.wr >= 0 && row + mk.wr + 1 < key_hi) key_hi = row + mk.wr + 1;
+        if (mk.wl >= 0) key_lo = row - mk.wl;
+      }
       int n_done = 0;
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits(mk, qt, chunk, n_q, n_kv);
+        uint32_t bits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
         while (bits != 0u && ok) {
           const int j = chunk * 32 + (__ffs(bits) - 1);
           bits &= bits - 1;
@@ -985,7 +997,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               kb[4 * g + 3] = kw.w;
             }
           }
-          const bool masked = tile_needs_element_mask(mk, qt, j, kv_len);
+          // WIN: whether this row's visible-key edge falls in the warpgroup's 32 columns
+          const bool masked = WIN ? (j * kTile + 32 * wg < key_lo || j * kTile + 32 * wg + 32 > key_hi)
+                                  : tile_needs_element_mask<WIN>(mk, qt, j, kv_len);
           // ---- P = exp2(S c - lse2), kept as bf16 pairs
           if (!mbar_wait_warp(bars.s_full, sc++ & 1, tmo, abort_flag)) {
             fail();
@@ -1015,7 +1029,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               p[c] = ex2_approx(x0);
               p[c + 1] = ex2_approx(x1);
             }
-            if (masked) {  // keys [0, lim) of this tile are allowed for this row
+            if constexpr (WIN) {
+              if (masked) {  // keys [key_lo, key_hi) are allowed for this row
+                const int base = j * kTile + 32 * wg;  // key of column 0 of this warpgroup
+                const int lim_local = key_hi - base, lo_local = key_lo - base;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) p[c] = (c >= lo_local && c < lim_local) ? p[c] : 0.f;
+              }
+            } else if (masked) {  // keys [0, lim) of this tile are allowed for this row
               int lim = kv_len - j * kTile;
               if (mk.causal) {
                 const int lc = row - j * kTile + 1;
@@ -1133,11 +1154,15 @@ template <int D>
 cudaError_t launch_dkdv_split_d(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
                                 bool dropout, int grid, cudaStream_t stream) {
-  const bool gqa = a.mask.Hkv != a.mask.H;
-  auto kern = dropout ? (gqa ? fa_bwd_dkdv_split_kernel<D, true, true>
-                             : fa_bwd_dkdv_split_kernel<D, true, false>)
-                      : (gqa ? fa_bwd_dkdv_split_kernel<D, false, true>
-                             : fa_bwd_dkdv_split_kernel<D, false, false>);
+  const bool gqa = a.mask.Hkv != a.mask.H, win = a.mask.wl >= 0 || a.mask.wr >= 0;
+  auto pick = [&](auto drop) {
+    constexpr bool DR = decltype(drop)::value;
+    return gqa ? (win ? fa_bwd_dkdv_split_kernel<D, DR, true, true>
+                      : fa_bwd_dkdv_split_kernel<D, DR, true, false>)
+               : (win ? fa_bwd_dkdv_split_kernel<D, DR, false, true>
+                      : fa_bwd_dkdv_split_kernel<D, DR, false, false>);
+  };
+  auto kern = dropout ? pick(std::true_type{}) : pick(std::false_type{});
   cudaError_t e = set_smem_split(kern, DkdvL<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, DkdvL<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
@@ -1148,7 +1173,11 @@ template <int D>
 cudaError_t launch_dq_split_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const BwdArgs& a, bool dropout, int grid,
                               cudaStream_t stream) {
-  auto kern = dropout ? fa_bwd_dq_split_kernel<D, true> : fa_bwd_dq_split_kernel<D, false>;
+  const bool win = a.mask.wl >= 0 || a.mask.wr >= 0;
+  auto kern = dropout ? (win ? fa_bwd_dq_split_kernel<D, true, true>
+                             : fa_bwd_dq_split_kernel<D, true, false>)
+                      : (win ? fa_bwd_dq_split_kernel<D, false, true>
+                             : fa_bwd_dq_split_kernel<D, false, false>);
   cudaError_t e = set_smem_split(kern, DqL<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, DqL<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);

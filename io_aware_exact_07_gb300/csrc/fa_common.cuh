@@ -22,6 +22,7 @@ struct MaskParams {
   int Hkv;                      // K/V heads (H for per-head attention; H / Hkv query heads share one)
   int nb;                       // ceil(N / 128): tiles per side, block-mask row length
   int causal;
+  int wl, wr;                   // sliding window: keys i - wl .. i + wr visible (-1: unbounded)
   const uint8_t* block_mask;    // [nb, nb] or null
   const int32_t* seqlens_k;     // [B] or null
 };
@@ -84,37 +85,56 @@ __device__ __forceinline__ int sched_unit(int k) {
 }
 
 // Whether the (query tile qt, key tile kt) pair has any allowed element.
-// n_kv = ceil(kv_len / 128), n_q = ceil(N / 128).
+// n_kv = ceil(kv_len / 128), n_q = ceil(N / 128). With a sliding window (WIN:
+// a separate kernel instance, so that kernels without one keep their code)
+// the pair is skipped when the band i - wl <= j <= i + wr misses the tile.
+template <bool WIN = false>
 __device__ __forceinline__ bool tile_valid(const MaskParams& m, int qt, int kt, int n_q,
                                            int n_kv) {
   if (qt >= n_q || kt >= n_kv) return false;
   if (m.causal && kt > qt) return false;
+  if constexpr (WIN) {
+    if (m.wl >= 0 && kt * kTile + (kTile - 1) + m.wl < qt * kTile) return false;
+    if (m.wr >= 0 && kt * kTile > qt * kTile + (kTile - 1) + m.wr) return false;
+  }
   if (m.block_mask != nullptr && m.block_mask[qt * m.nb + kt] == 0) return false;
   return true;
 }
 
-// Whether the pair needs a per-element mask (causal diagonal, or key tile
-// crossing kv_len). Query rows beyond N are never written, so the query tail
-// needs none.
+// Whether the pair needs a per-element mask (causal diagonal, key tile
+// crossing kv_len, or a sliding-window edge inside the tile). Query rows
+// beyond N are never written, so the query tail needs none.
+template <bool WIN = false>
 __device__ __forceinline__ bool tile_needs_element_mask(const MaskParams& m, int qt, int kt,
                                                         int kv_len) {
+  if constexpr (WIN) {
+    if (m.wl >= 0 && kt * kTile < qt * kTile + (kTile - 1) - m.wl) return true;
+    if (m.wr >= 0 && kt * kTile + (kTile - 1) > qt * kTile + m.wr) return true;
+  }
   return (m.causal && kt == qt) || ((kt + 1) * kTile > kv_len);
+}
+
+// Whether key j is inside query i's sliding window.
+__device__ __forceinline__ bool in_window(const MaskParams& m, int i, int j) {
+  return (m.wl < 0 || j >= i - m.wl) && (m.wr < 0 || j <= i + m.wr);
 }
 
 // Bits j in [32*c, 32*c + 32) that are valid for query tile qt, computed by a
 // whole warp (one candidate per lane).
+template <bool WIN = false>
 __device__ __forceinline__ uint32_t warp_valid_bits(const MaskParams& m, int qt, int chunk,
                                                     int n_q, int n_kv) {
   const int lane = threadIdx.x & 31;
-  const bool v = tile_valid(m, qt, chunk * 32 + lane, n_q, n_kv);
+  const bool v = tile_valid<WIN>(m, qt, chunk * 32 + lane, n_q, n_kv);
   return __ballot_sync(0xffffffffu, v);
 }
 
 // Same, transposed: query tiles qt in [32*c, 32*c + 32) valid for key tile kt.
+template <bool WIN = false>
 __device__ __forceinline__ uint32_t warp_valid_bits_t(const MaskParams& m, int kt, int chunk,
                                                       int n_q, int n_kv) {
   const int lane = threadIdx.x & 31;
-  const bool v = tile_valid(m, chunk * 32 + lane, kt, n_q, n_kv);
+  const bool v = tile_valid<WIN>(m, chunk * 32 + lane, kt, n_q, n_kv);
   return __ballot_sync(0xffffffffu, v);
 }
 

@@ -100,7 +100,7 @@ __device__ __forceinline__ UnitCoord decode_unit(int u, int BH, int H, int n_qbl
 
 }  // namespace
 
-template <int D, bool DROPOUT>
+template <int D, bool DROPOUT, bool WIN>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
@@ -224,8 +224,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       ++q_armed;
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits(mk, uc.qt0, chunk, n_q, n_kv) |
-                        warp_valid_bits(mk, uc.qt0 + 1, chunk, n_q, n_kv);
+        uint32_t bits = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv) |
+                        warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
         while (bits != 0u) {
           const int j = chunk * 32 + (__ffs(bits) - 1);
           bits &= bits - 1;
@@ -349,8 +349,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        const uint32_t va = warp_valid_bits(mk, uc.qt0, chunk, n_q, n_kv);
-        const uint32_t vb = warp_valid_bits(mk, uc.qt0 + 1, chunk, n_q, n_kv);
+        const uint32_t va = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv);
+        const uint32_t vb = warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
         if (leader) {
           uint32_t bits = va | vb;
           while (bits != 0u && ok) {
@@ -490,8 +490,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           return true;
         };
         for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-          const uint32_t va = warp_valid_bits(mk, uc.qt0, chunk, n_q, n_kv);
-          const uint32_t vb = warp_valid_bits(mk, uc.qt0 + 1, chunk, n_q, n_kv);
+          const uint32_t va = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv);
+          const uint32_t vb = warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
           if (leader) {
             uint32_t bits = va | vb;
             while (bits != 0u && ok) {
@@ -550,13 +550,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int n_kv = (kv_len + kTile - 1) / kTile;
       int jmax = n_kv;
       if (mk.causal && qt + 1 < jmax) jmax = qt + 1;
+      // sliding window: keys [key_lo, key_hi) are visible to this row
+      int key_lo = 0, key_hi = kv_len;
+      if constexpr (WIN) {
+        if (mk.causal && row + 1 < key_hi) key_hi = row + 1;
+        if (mk.wr >= 0 && row + mk.wr + 1 < key_hi) key_hi = row + mk.wr + 1;
+        if (mk.wl >= 0) key_lo = row - mk.wl;
+      }
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
       float l_sum = 0.f;        // running sum of exp2(s*c - m_ref), undropped
       int n_done = 0;
       const uint32_t row_global = static_cast<uint32_t>(uc.bh) * static_cast<uint32_t>(N) +
                                   static_cast<uint32_t>(row);
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits(mk, qt, chunk, n_q, n_kv);
+        uint32_t bits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
         while (bits != 0u) {
           const int j = chunk * 32 + (__ffs(bits) - 1);
           bits &= bits - 1;
@@ -579,7 +586,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           float s[128];
 #pragma unroll
           for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(sr[k]);
-          if (tile_needs_element_mask(mk, qt, j, kv_len)) {
+          if constexpr (WIN) {
+            if (j * kTile < key_lo || (j + 1) * kTile > key_hi) {  // this row's edge is in the tile
+              const int lim = key_hi - j * kTile, lo = key_lo - j * kTile;  // keys [lo, lim) valid
+#pragma unroll
+              for (int k = 0; k < 128; ++k)
+                if (k >= lim || k < lo) s[k] = -INFINITY;
+            }
+          } else if (tile_needs_element_mask<WIN>(mk, qt, j, kv_len)) {
             int lim = kv_len - j * kTile;                 // keys [0, lim) of this tile are valid
             if (mk.causal) {
               const int lc = row - j * kTile + 1;       // causal: key <= row
@@ -752,7 +766,8 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const FwdArgs& a, int grid,
                                    cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fa_fwd_kernel<D, DROPOUT>;
+  const bool win = a.mask.wl >= 0 || a.mask.wr >= 0;
+  auto kern = win ? fa_fwd_kernel<D, DROPOUT, true> : fa_fwd_kernel<D, DROPOUT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        L::kSmemBytes);
   if (e != cudaSuccess) return e;

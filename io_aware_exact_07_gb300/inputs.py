@@ -33,6 +33,7 @@ class Workload:
     butterfly: bool = False
     seed: int = 0
     Hkv: int | None = None  # K/V heads (grouped-query attention); None: one per query head
+    window: tuple = (-1, -1)  # sliding window (left, right); -1: that side unbounded
     description: str = field(default="", compare=False)
 
     @property
@@ -66,7 +67,14 @@ SPARSE = Workload("butterfly_16k", 4, 16, 16384, 64, butterfly=True,
 GQA_CAUSAL = Workload("gqa_causal_4k", 8, 32, 4096, 128, causal=True, Hkv=8,
                       description="B=8 H=32 H_kv=8 N=4096 d=128, causal, grouped K/V heads")
 
-ALL = {w.name: w for w in (TINY, GPT2_MEDIUM, CAUSAL, LONG_D64, LONG_D128, SPARSE, GQA_CAUSAL)}
+# Sliding-window (local) attention, which the pages list among the variants
+# and the block-skipping patterns without a workload: a long causal sequence
+# where each query sees the 4096 keys ending at itself.
+SLIDING = Workload("sliding_16k", 2, 32, 16384, 128, causal=True, window=(4095, -1),
+                   description="B=2 H=32 N=16384 d=128, causal, sliding window of 4096 keys")
+
+ALL = {w.name: w for w in (TINY, GPT2_MEDIUM, CAUSAL, LONG_D64, LONG_D128, SPARSE, GQA_CAUSAL,
+                           SLIDING)}
 
 
 def draw(w: Workload, with_grad: bool = True):
