@@ -283,3 +283,95 @@ def fwd_decode(q, k, v, scale, causal=False, seqlens_k=None, heads=None):
             o[b, h, i] = (e @ vh[:n]) / den
             lse[b, h, i] = m + np.log(den)
     return o, lse
+
+
+# ------------------------------------------------------------------ FP8 forward
+# The cross-paper synthesis page on FlashAttention (section 2, the FA-3 entry)
+# names FP8 with incoherent processing as FA-3's third Hopper technique. Read
+# plainly: Q and K are multiplied by the same random orthogonal matrix M (a
+# Hadamard matrix with random signs), which leaves Q K^T unchanged while
+# spreading outlier channels, and Q, K, V are then stored as 8-bit floats
+# (e4m3) with scales. The functions below restate those steps in fp64.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of e4m3 byte codes: sign bit, 4 exponent bits (bias 7), 3
+    mantissa bits; exponent 0 holds the subnormals 2^-6 * m/8; 0x7F / 0xFF
+    are NaN (the format has no infinities)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+_E4M3_POS = e4m3_decode(np.arange(0x7F, dtype=np.uint8))  # the 127 finite magnitudes, ascending
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest e4m3 code to each finite x, ties to the even code (the one with
+    mantissa bit 0), magnitudes above 448 saturated to 448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.searchsorted(_E4M3_POS, a, side="left")  # first magnitude >= a
+    hi = np.minimum(hi, len(_E4M3_POS) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E4M3_POS[hi] - a
+    d_lo = a - _E4M3_POS[lo]
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(x < 0, code | 0x80, code).astype(np.uint8)
+
+
+def hadamard(d: int) -> np.ndarray:
+    """Sylvester's Hadamard matrix of order d (a power of two): H_1 = [1],
+    H_2n = [[H_n, H_n], [H_n, -H_n]]."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def rotate(x, signs) -> np.ndarray:
+    """x M with M = diag(signs) H / sqrt(d): an orthogonal matrix, so
+    (q M)(k M)^T = q k^T; applied along the last axis."""
+    x = _f64(x)
+    d = x.shape[-1]
+    return (x * np.asarray(signs, dtype=np.float64)) @ hadamard(d) / np.sqrt(d)
+
+
+def quantize_fp8(q, k, v, signs):
+    """Quantisation for the FP8 forward, [B, H, N, d] inputs:
+      Q' = Q M, K' = K M; per-head scales s_q = amax|Q'| / 448, s_k likewise;
+      per-(head, column) scales s_v[c] = amax_rows |V[:, c]| / 448;
+      codes = nearest e4m3 of Q' / s_q, K' / s_k, V / s_v (a zero amax gives
+      scale 1). Returns (q8, k8, v8 uint8 [B, H, N, d], s_q, s_k [B, H],
+      s_v [B, H, d])."""
+    qr, kr, v = rotate(q, signs), rotate(k, signs), _f64(v)
+
+    def scale_of(amax):
+        return np.where(amax > 0, amax / E4M3_MAX, 1.0)
+
+    s_q = scale_of(np.abs(qr).max(axis=(2, 3)))
+    s_k = scale_of(np.abs(kr).max(axis=(2, 3)))
+    s_v = scale_of(np.abs(v).max(axis=2))
+    q8 = e4m3_encode(qr / s_q[:, :, None, None])
+    k8 = e4m3_encode(kr / s_k[:, :, None, None])
+    v8 = e4m3_encode(v / s_v[:, :, None, :])
+    return q8, k8, v8, s_q, s_k, s_v
+
+
+def fwd_fp8(q8, k8, v8, s_q, s_k, s_v, scale, causal=False, seqlens_k=None):
+    """Exact attention (the forward above, fp64) of the dequantised inputs
+    Q^ = dec(q8) s_q, K^ = dec(k8) s_k, V^ = dec(v8) s_v: what the FP8 kernel
+    computes before its own rounding of P. q8, k8, v8: uint8 [B, H, N, d]."""
+    qh = e4m3_decode(q8) * np.asarray(s_q, dtype=np.float64)[:, :, None, None]
+    kh = e4m3_decode(k8) * np.asarray(s_k, dtype=np.float64)[:, :, None, None]
+    vh = e4m3_decode(v8) * np.asarray(s_v, dtype=np.float64)[:, :, None, :]
+    return fwd(qh, kh, vh, scale, causal=causal, seqlens_k=seqlens_k)
