@@ -340,15 +340,18 @@ def hadamard(d: int) -> np.ndarray:
 
 def rotate(x, signs) -> np.ndarray:
     """x M with M = diag(signs) H / sqrt(d): an orthogonal matrix, so
-    (q M)(k M)^T = q k^T; applied along the last axis."""
+    (q M)(k M)^T = q k^T; applied along the last axis. signs None: no
+    rotation (M = I), the FP8 path without incoherent processing."""
     x = _f64(x)
+    if signs is None:
+        return x
     d = x.shape[-1]
     return (x * np.asarray(signs, dtype=np.float64)) @ hadamard(d) / np.sqrt(d)
 
 
 def quantize_fp8(q, k, v, signs):
     """Quantisation for the FP8 forward, [B, H, N, d] inputs:
-      Q' = Q M, K' = K M; per-head scales s_q = amax|Q'| / 448, s_k likewise;
+      Q' = Q M, K' = K M (M = I when signs is None); per-head scales s_q = amax|Q'| / 448, s_k likewise;
       per-(head, column) scales s_v[c] = amax_rows |V[:, c]| / 448;
       codes = nearest e4m3 of Q' / s_q, K' / s_k, V / s_v (a zero amax gives
       scale 1). Returns (q8, k8, v8 uint8 [B, H, N, d], s_q, s_k [B, H],

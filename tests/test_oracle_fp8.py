@@ -118,3 +118,12 @@ def test_fp8_forward_on_representable_inputs_is_the_plain_forward():
     vh = oracle.e4m3_decode(v8) * sv[:, :, None, :]
     o2, lse2 = oracle.fwd(qh, kh, vh, 0.25, causal=True)
     assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def test_no_rotation_quantises_the_inputs_themselves():
+    r = rng(34)
+    q, k, v = r.standard_normal((3, 1, 2, 40, 16))
+    q8, k8, v8, sq, sk, sv = oracle.quantize_fp8(q, k, v, None)
+    assert np.array_equal(q8, oracle.e4m3_encode(q / sq[:, :, None, None]))
+    assert np.array_equal(k8, oracle.e4m3_encode(k / sk[:, :, None, None]))
+    assert np.allclose(sq, np.abs(q).max(axis=(2, 3)) / 448.0, rtol=1e-15)
