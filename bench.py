@@ -707,6 +707,180 @@ def run_decode_reference(args, w):
     }
 
 
+# --------------------------------------------------------------- FP8 workload
+
+FP8_METRIC = "attention fwd TFLOP/s (FP8 e4m3 operands, fp32 accumulation)"
+
+
+def run_fp8(args, w):
+    """FP8 forward on the causal decoder shape: bf16 inputs quantised once by
+    fa_fp8_quantize (timed separately), then fa_fwd_fp8 timed per step."""
+    world, rank, local, pg = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import io_aware_exact_07_gb300 as fa
+    x = inputs.draw(w, with_grad=False)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    signs = inputs.rotation_signs(w.d, seed=0).to(dev)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    Np = fa.fa_fp8_vt_stride(N)
+    z = dict(q8=torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
+             k8=torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
+             vt8=torch.empty((B, H, d, Np), dtype=torch.uint8, device=dev),
+             s_q=torch.empty((B, H), dtype=torch.float32, device=dev),
+             s_k=torch.empty((B, H), dtype=torch.float32, device=dev),
+             s_v=torch.empty((B, H, d), dtype=torch.float32, device=dev))
+    wsb = fa.fa_fp8_workspace_size(B, H, d)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+    def quant():
+        st = fa.fa_fp8_quantize(q, k, v, signs, B, H, N, d, z["q8"], z["k8"], z["vt8"], z["s_q"],
+                                z["s_k"], z["s_v"], ws, wsb)
+        if st != 0:
+            raise RuntimeError(f"fa_fp8_quantize failed with status {st}")
+
+    def fwd():
+        st = fa.fa_fwd_fp8(z["q8"], z["k8"], z["vt8"], z["s_q"], z["s_k"], z["s_v"], o, lse, B,
+                           H, N, d, w.scale, w.causal)
+        if st != 0:
+            raise RuntimeError(f"fa_fwd_fp8 failed with status {st}")
+
+    pairs = allowed_pairs(w, None)
+    flops = 4.0 * w.d * pairs
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        quant()
+        fwd()
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0, "device-side error during warm-up"
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    q0.record(stream)
+    for _ in range(10):
+        quant()
+    q1.record(stream)
+    torch.cuda.synchronize()
+    t_quant = q0.elapsed_time(q1) / 10 / 1e3
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            fwd()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(pg)
+    elapsed = max_over_ranks(pg, start.elapsed_time(end) / 1e3)
+    assert fa.fa_device_status() == 0, "device-side error during the timed region"
+    e2e = None
+    if not args.no_e2e:
+        # per step: bf16 Q, K, V in from pinned host memory, quantise, forward, O and lse out
+        hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        n = max(3, min(args.steps, 10))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n):
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            quant()
+            fwd()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        secs = max_over_ranks(pg, a0.elapsed_time(a1) / 1e3)
+        e2e = {"value": flops * n * world / secs / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 3 * q.numel() * 2,
+               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4, "steps": n}
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return None
+    peaks, peak_src = load_peaks()
+    # FP8 dense peak: the measured bf16 peak times the nominal FP8 / bf16 ratio (2)
+    peak8 = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    t_step = elapsed / args.steps
+    value = flops * args.steps * world / elapsed / 1e12
+    qbytes = 2 * 3 * B * H * N * d * 2 + 3 * B * H * N * d  # bf16 read by both passes, e4m3 written
+    result = {
+        "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded N(0,1) bf16 Q, K, V quantised by the library; no dataset)",
+        "config": {"workload": w.name, "description": w.description, "B": B, "H": H, "N": N,
+                   "d": d, "causal": w.causal, "allowed_pairs": pairs, "flops_per_step": flops,
+                   "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world} (no collective)"},
+        "breakdown": {"fwd_ms": t_step * 1e3, "quantise_ms": t_quant * 1e3,
+                      "quantise_gbs": qbytes / t_quant / 1e9},
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak8,
+                     "unit": "TFLOP/s", "frac": value / world / peak8, "traffic": None,
+                     "kernel": "fa_fwd_fp8_kernel",
+                     "peak_source": f"{peak_src} (bf16_tflops x 2, the nominal FP8 ratio)"},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        z_cpu = {n_: t.cpu() for n_, t in z.items()}
+        t0 = time.perf_counter()
+        heads = 0
+        v8 = z_cpu["vt8"][..., :N].transpose(2, 3).contiguous()
+        while time.perf_counter() - t0 < 10.0 and heads < B * H:
+            b, h = divmod(heads, H)
+            sl = lambda t: t[b:b + 1, h:h + 1].numpy()
+            oracle.fwd_fp8(sl(z_cpu["q8"]), sl(z_cpu["k8"]), sl(v8), sl(z_cpu["s_q"]).astype(np.float64),
+                           sl(z_cpu["s_k"]).astype(np.float64), sl(z_cpu["s_v"]).astype(np.float64),
+                           w.scale, causal=w.causal)
+            heads += 1
+        secs = time.perf_counter() - t0
+        cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+        result["cpu_baseline"] = {"value": flops / (B * H) * heads / secs / 1e12, "unit": "TFLOP/s",
+                                  "cores": cores, "kind": "oracle",
+                                  "sample": f"{heads} of {B * H} heads of {w.name}, fp64, {secs:.1f} s"}
+    if pg is not None:
+        pg.destroy_process_group()
+    return result
+
+
+def run_fp8_reference(args, w):
+    """The fp64 oracle's FP8 forward (exact attention of the dequantised
+    inputs) on the host, head (0, 0) per step."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    import oracle
+    x = inputs.draw(inputs.Workload("s", 1, 1, w.N, w.d, causal=w.causal), with_grad=False)
+    f64 = lambda t: t.double().numpy()
+    signs = inputs.rotation_signs(w.d, seed=0).double().numpy()
+    q8, k8, v8, sq, sk, sv = oracle.quantize_fp8(f64(x["q"]), f64(x["k"]), f64(x["v"]), signs)
+    for _ in range(args.warmup):
+        oracle.fwd_fp8(q8, k8, v8, sq, sk, sv, w.scale, causal=w.causal)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fwd_fp8(q8, k8, v8, sq, sk, sv, w.scale, causal=w.causal)
+    secs = time.perf_counter() - t0
+    flops = 4.0 * w.d * allowed_pairs(inputs.Workload("s", 1, 1, w.N, w.d, causal=w.causal), None)
+    value = flops * args.steps / secs / 1e12
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {
+        "impl": "reference", "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), same recipe)",
+        "config": {"workload": w.name, "description": w.description},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one head of {w.name} per step, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,12 +888,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(inputs.ALL) + [inputs.DECODE.name])
+                    choices=sorted(inputs.ALL) + [inputs.DECODE.name, inputs.FP8_CAUSAL.name])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
-    if args.workload == inputs.DECODE.name:
+    if args.workload == inputs.FP8_CAUSAL.name:
+        w = inputs.FP8_CAUSAL
+        res = run_fp8_reference(args, w) if args.impl == "reference" else run_fp8(args, w)
+    elif args.workload == inputs.DECODE.name:
         w = inputs.DECODE
         res = run_decode_reference(args, w) if args.impl == "reference" else run_decode(args, w)
     else:

@@ -215,6 +215,45 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
                     const int32_t* seqlens_k, int num_ctas, void* workspace,
                     size_t workspace_bytes, void* stream);
 
+/* FP8 forward with incoherent processing (FA-3's FP8 path, which the
+ * cross-paper synthesis page on FlashAttention names in its section 2), head
+ * dimension 128, forward only.
+ * fa_fp8_quantize: Q' = Q M and K' = K M with M = diag(signs) H / sqrt(128),
+ *   H the Sylvester Hadamard matrix (signs: fp32 [128] of +-1, device; NULL
+ *   means no rotation), each stored as e4m3 codes with one scale per head,
+ *   s = amax / 448 (1 for an all-zero head); V as e4m3 with one scale per
+ *   (head, column), written transposed.
+ *     q, k, v:  bf16 [B, H, N, 128] (device, 16-byte aligned)
+ *     q8, k8:   uint8 [B, H, N, 128] (e4m3 codes, rounded to nearest even,
+ *               saturating at 448)
+ *     vt8:      uint8 [B, H, 128, Np], Np = fa_fp8_vt_stride(N) (N rounded up
+ *               to 16; keys N .. Np-1 are written as zero)
+ *     s_q, s_k: fp32 [B, H]; s_v: fp32 [B, H, 128]
+ *     workspace: fa_fp8_workspace_size(B, H, 128) bytes (device, 16-byte aligned)
+ * fa_fwd_fp8: attention of Q^ = dec(q8) s_q, K^ = dec(k8) s_k, V^ = dec(vt8)^T s_v
+ *   (rotated Q and K give the same scores), both products on the tensor core
+ *   in FP8 with fp32 accumulation; P is rounded to e4m3 for the PV product
+ *   (kept between 2^7 and 2^8 at each row's maximum, so weights down to 2^-16
+ *   of it are represented). Causal and key padding as fa_fwd. o: bf16
+ *   [B, H, N, 128]; lse: fp32 [B, H, N] (natural log).
+ * Accuracy contract (the exactness of fa_fwd does not carry over): against
+ * exact attention of the dequantised inputs, |O - O^| <= 2^-4 sum_j P_ij |v^_j|
+ * + 2^-17 sum_j |v^_j| (the e4m3 rounding of P, with underflow below 2^-9)
+ * + 1.5 bf16 half-ulps of O; lse within 1e-3. Against the bf16 inputs the
+ * error adds the quantisation of Q, K, V, which the rotation reduces when
+ * channels carry outliers.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (d != 128), FA_ERR_WORKSPACE,
+ * FA_ERR_CUDA. Asynchronous on `stream`; nothing is allocated. */
+size_t fa_fp8_workspace_size(int B, int H, int d);
+int fa_fp8_vt_stride(int N);
+fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs, int B,
+                          int H, int N, int d, void* q8, void* k8, void* vt8, float* s_q,
+                          float* s_k, float* s_v, void* workspace, size_t workspace_bytes,
+                          void* stream);
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s_q,
+                     const float* s_k, const float* s_v, void* o, float* lse, int B, int H, int N,
+                     int d, float scale, int causal, const int32_t* seqlens_k, void* stream);
+
 /* Quantised dropout threshold round(256 p) used by fa_fwd / fa_bwd (-1 if p is
  * outside [0, 1)). The effective dropout rate is fa_dropout_p8(p) / 256. */
 int fa_dropout_p8(float dropout_p);

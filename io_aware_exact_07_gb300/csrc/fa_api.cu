@@ -108,6 +108,25 @@ bool encode_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [outer, rows, inner] tensor of bytes (e4m3 codes) with rows of `inner`
+// bytes spaced `row_stride` bytes apart: 128-byte x 128-row boxes, 128-byte
+// swizzle, out-of-range elements read as zero.
+bool encode_map_u8(CUtensorMap* m, const void* base, int outer, int rows, int inner,
+                   int row_stride) {
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(row_stride)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 fa::MaskParams make_mask(int B, int H, int Hkv, int N, int causal, const uint8_t* bm,
                          const int32_t* sl, int wl = -1, int wr = -1) {
   fa::MaskParams m;
@@ -506,6 +525,85 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
   cudaError_t e = fa::launch_decode(tq, tk, tv, a, d, p.grid, s);
   if (e == cudaSuccess && p.seg_max > 1) e = fa::launch_decode_combine(a, d, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_fp8_workspace_size(int B, int H, int d) {
+  if (B < 1 || H < 1 || d != 128) return 0;
+  return round256(static_cast<size_t>(B) * H * (2 + 128) * sizeof(unsigned int));
+}
+
+int fa_fp8_vt_stride(int N) { return N < 1 ? 0 : (N + 15) / 16 * 16; }
+
+fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs, int B,
+                          int H, int N, int d, void* q8, void* k8, void* vt8, float* s_q,
+                          float* s_k, float* s_v, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, v, q8, k8, vt8, s_q, s_k, s_v};  // signs may be null
+  for (const void* p : ptrs)
+    if (p == nullptr) return FA_ERR_INVALID_ARG;
+  const void* tensors[] = {q, k, v, q8, k8, vt8};
+  for (const void* p : tensors)
+    if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < fa_fp8_workspace_size(B, H, d) ||
+      !aligned16(workspace))
+    return FA_ERR_WORKSPACE;
+  DeviceInfo* di = nullptr;
+  fa_status st = device_info(&di);
+  if (st != FA_OK) return st;
+  fa::Fp8QuantArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.signs = signs;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.Np = fa_fp8_vt_stride(N);
+  a.amax = static_cast<unsigned int*>(workspace);
+  a.q8 = static_cast<uint8_t*>(q8);
+  a.k8 = static_cast<uint8_t*>(k8);
+  a.vt8 = static_cast<uint8_t*>(vt8);
+  a.s_q = s_q;
+  a.s_k = s_k;
+  a.s_v = s_v;
+  return fa::launch_fp8_quantize(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s_q,
+                     const float* s_k, const float* s_v, void* o, float* lse, int B, int H, int N,
+                     int d, float scale, int causal, const int32_t* seqlens_k, void* stream) {
+  fa_status st = check_common(B, H, N, d, scale, 0.f, H);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!q8 || !k8 || !vt8 || !s_q || !s_k || !s_v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o))
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  const int Np = fa_fp8_vt_stride(N);
+  CUtensorMap tq, tk, tv;
+  if (!encode_map_u8(&tq, q8, B * H, N, 128, 128) || !encode_map_u8(&tk, k8, B * H, N, 128, 128) ||
+      !encode_map_u8(&tv, vt8, B * H, 128, Np, Np))
+    return FA_ERR_CUDA;
+  fa::Fp8FwdArgs a;
+  a.mask = make_mask(B, H, H, N, causal, nullptr, seqlens_k);
+  a.sync = make_sync(di, false);
+  a.scale_log2 = scale * fa::kLog2e;
+  a.s_q = s_q;
+  a.s_k = s_k;
+  a.s_v = s_v;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  return fa::launch_fwd_fp8(tq, tk, tv, a, di->num_sms, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
 }
 
 int fa_dropout_p8(float dropout_p) { return p8_of(dropout_p); }

@@ -57,6 +57,31 @@ cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const DecodeArgs& a, int d, int grid, cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeArgs& a, int d, cudaStream_t stream);
 
+// FP8 forward (fa_fp8.cu, fa_fwd_fp8.cu), head dimension 128.
+struct Fp8QuantArgs {
+  const __nv_bfloat16 *q, *k, *v;  // [B, H, N, 128]
+  const float* signs;              // [128], +-1: the rotation's random signs
+  int B, H, N, Np;                 // Np: row stride of vt8, N rounded up to 16
+  unsigned int* amax;              // workspace [B*H*130]
+  uint8_t *q8, *k8;                // e4m3 [B, H, N, 128] (rotated, scaled)
+  uint8_t* vt8;                    // e4m3 [B, H, 128, Np] (V transposed, scaled per column)
+  float *s_q, *s_k;                // [B*H]
+  float* s_v;                      // [B*H, 128]
+};
+
+struct Fp8FwdArgs {
+  MaskParams mask;
+  SyncParams sync;
+  float scale_log2;                // softmax scale * log2(e)
+  const float *s_q, *s_k, *s_v;
+  __nv_bfloat16* o;                // [B, H, N, 128]
+  float* lse;                      // [B, H, N]
+};
+
+cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                           const Fp8FwdArgs& a, int num_sms, cudaStream_t stream);
+
 // Tensor maps of a [B*H, N, d] bf16 tensor with 128 x 64 boxes, 128-byte swizzle.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, int d, bool dropout, int num_sms, cudaStream_t stream);

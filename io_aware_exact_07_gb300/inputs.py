@@ -156,3 +156,31 @@ def sample_heads(w: Workload, count: int = 4, seed: int = 1234):
         if hb not in heads:
             heads.append(hb)
     return heads
+
+
+# FP8 forward: the causal decoder shape, bf16 inputs quantised by the library.
+FP8_CAUSAL = Workload("fp8_causal_4k", 8, 32, 4096, 128, causal=True,
+                      description="B=8 H=32 N=4096 d=128, causal, FP8 (e4m3) forward with "
+                                  "Hadamard rotation")
+
+
+def rotation_signs(d: int, seed: int = 0) -> torch.Tensor:
+    """+-1 fp32 [d]: the random signs of the FP8 path's rotation, drawn once."""
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randint(0, 2, (d,), generator=g) * 2 - 1).to(torch.float32)
+
+
+def draw_fp8_codes(B, H, N, d, seed=0):
+    """Random e4m3 codes for the FP8 forward: q8, k8, v8 uint8 [B, H, N, d] as the
+    bytes of N(0, 1) * 64 rounded to e4m3 by torch (magnitudes up to ~300, so
+    most of the code range is used), and positive scales s_q, s_k [B, H],
+    s_v [B, H, d] drawn uniformly from [0.003, 0.012]."""
+    g = torch.Generator().manual_seed(seed)
+    out = {}
+    for name in ("q8", "k8", "v8"):
+        x = torch.randn((B, H, N, d), generator=g) * 64.0
+        out[name] = x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    out["s_q"] = torch.rand((B, H), generator=g) * 0.009 + 0.003
+    out["s_k"] = torch.rand((B, H), generator=g) * 0.009 + 0.003
+    out["s_v"] = torch.rand((B, H, d), generator=g) * 0.009 + 0.003
+    return out
