@@ -98,10 +98,28 @@ def load_peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
-def kernel_source_hash():
+# Sources each timed kernel is built from: a committed DRAM-traffic figure is
+# used only while these files are unchanged since it was captured.
+KERNEL_SOURCES = {
+    "fwd": ("fa_fwd.cu",),
+    "bwd_dkdv": ("fa_bwd.cu", "fa_bwd_split.cu"),
+    "bwd_dq": ("fa_bwd_split.cu",),
+    "bwd_preprocess": ("fa_bwd.cu",),
+    "decode": ("fa_decode.cu",),
+    "fwd_fp8": ("fa_fwd_fp8.cu",),
+}
+COMMON_SOURCES = ("fa_common.cuh", "sm103_ptx.cuh", "fa_kernels.h")
+
+
+def kernel_source_hash(kernel=None):
+    """sha256 (16 hex digits) of the CUDA sources a kernel is built from (all of
+    them when the kernel is not listed)."""
+    csrc = os.path.join(ROOT, "io_aware_exact_07_gb300", "csrc")
+    names = sorted(os.listdir(csrc)) if kernel not in KERNEL_SOURCES else \
+        sorted(KERNEL_SOURCES[kernel] + COMMON_SOURCES)
     h = hashlib.sha256()
-    for name in sorted(os.listdir(os.path.join(ROOT, "io_aware_exact_07_gb300", "csrc"))):
-        with open(os.path.join(ROOT, "io_aware_exact_07_gb300", "csrc", name), "rb") as f:
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
@@ -113,7 +131,7 @@ def ncu_traffic(kernel: str, workload: str):
         with open(path) as f:
             t = json.load(f)
         e = t[workload][kernel]
-        if e.get("source_hash") != kernel_source_hash():
+        if e.get("source_hash") != kernel_source_hash(kernel):
             return None
         return float(e["bytes_per_launch"])
     except Exception:
@@ -318,9 +336,26 @@ def cpu_baseline(w, x, seqlens, budget_s=15.0):
         pairs += allowed_pairs(wb, None if seqlens is None else [int(seqlens[b])])
     flops = 14.0 * w.d * pairs
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": flops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{n} of {w.B * w.H} heads of {w.name}, fwd+bwd in fp64, {t:.1f} s",
             "seconds": t}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (for the CPU-baseline line), or the machine type."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
 
 
 def measure_e2e(step, x, pg, stream, n_steps):
@@ -510,7 +545,7 @@ def run_reference(args, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), same inputs)",
         "config": {"workload": w.name, "description": w.description, "allowed_pairs": pairs,
                    "flops_per_step": flops},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -673,7 +708,7 @@ def decode_cpu_baseline(w, x, budget_s=12.0):
     # numpy's matrix-vector products run in its BLAS, which may use every core
     cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS",
                                                                       os.cpu_count() or 1)))
-    return {"value": byts / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+    return {"value": byts / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{n} of {len(groups)} K/V groups of {w.name} (all their query heads)"
                       f"{f' x{reps}' if reps > 1 else ''}, fp64 numpy (BLAS threads up to "
                       f"{cores}), {t:.1f} s", "seconds": t}
@@ -700,7 +735,7 @@ def run_decode_reference(args, w):
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), same inputs)",
         "config": {"workload": w.name, "description": w.description, "bytes_per_step": byts},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cb["cores"], "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -819,7 +854,8 @@ def run_fp8(args, w):
         "breakdown": {"fwd_ms": t_step * 1e3, "quantise_ms": t_quant * 1e3,
                       "quantise_gbs": qbytes / t_quant / 1e9},
         "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak8,
-                     "unit": "TFLOP/s", "frac": value / world / peak8, "traffic": None,
+                     "unit": "TFLOP/s", "frac": value / world / peak8,
+                     "traffic": ncu_traffic("fwd_fp8", w.name),
                      "kernel": "fa_fwd_fp8_kernel",
                      "peak_source": f"{peak_src} (bf16_tflops x 2, the nominal FP8 ratio)"},
         "e2e": e2e,
@@ -842,7 +878,7 @@ def run_fp8(args, w):
         secs = time.perf_counter() - t0
         cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
         result["cpu_baseline"] = {"value": flops / (B * H) * heads / secs / 1e12, "unit": "TFLOP/s",
-                                  "cores": cores, "kind": "oracle",
+                                  "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
                                   "sample": f"{heads} of {B * H} heads of {w.name}, fp64, {secs:.1f} s"}
     if pg is not None:
         pg.destroy_process_group()
@@ -874,7 +910,7 @@ def run_fp8_reference(args, w):
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), same recipe)",
         "config": {"workload": w.name, "description": w.description},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": f"one head of {w.name} per step, fp64"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
