@@ -243,7 +243,7 @@ def bwd_gqa(q, k, v, dout, scale, **kw):
     return dq, dk, dv, D
 
 
-def fwd_decode(q, k, v, scale, causal=False, seqlens_k=None, heads=None):
+def fwd_decode(q, k, v, scale, causal=False, seqlens_k=None, heads=None, window_left=-1):
     """Attention of a short block of new query rows over a key/value cache, in
     fp64: the decode case that the page "FlashAttention — L3 Cross-Paper
     Synthesis" (section 3, the attack surface) names as left unoptimised,
@@ -258,6 +258,8 @@ def fwd_decode(q, k, v, scale, causal=False, seqlens_k=None, heads=None):
     softmax attention: scores scale * q . k_j over the allowed keys, their
     softmax, the weighted sum of V rows, and lse = log of the softmax
     denominator. A row with no allowed key has O = 0, lse = -inf.
+    window_left >= 0 adds the sliding window: row i then sees only keys
+    j >= L_b - Nq + i - window_left as well.
 
     heads: optional list of (b, h) to compute; the others stay O = 0,
     lse = -inf. Returns (o [B, H, Nq, d], lse [B, H, Nq])."""
@@ -274,13 +276,14 @@ def fwd_decode(q, k, v, scale, causal=False, seqlens_k=None, heads=None):
         kh, vh = k[b, h // G], v[b, h // G]
         for i in range(Nq):
             n = min(L, L - Nq + i + 1) if causal else L  # allowed keys are j < n
-            if n <= 0:
+            j0 = max(0, L - Nq + i - window_left) if window_left >= 0 else 0  # ... and j >= j0
+            if n <= j0:
                 continue
-            s = scale * (kh[:n] @ q[b, h, i])
+            s = scale * (kh[j0:n] @ q[b, h, i])
             m = s.max()
             e = np.exp(s - m)
             den = e.sum()
-            o[b, h, i] = (e @ vh[:n]) / den
+            o[b, h, i] = (e @ vh[j0:n]) / den
             lse[b, h, i] = m + np.log(den)
     return o, lse
 

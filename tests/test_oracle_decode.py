@@ -134,3 +134,32 @@ def test_matches_torch_sdpa_fp64(H, Hkv, Nq, causal):
         assert np.max(np.abs(o[b][:, rows[b]] - ref[b][:, rows[b]])) < 1e-12
         assert np.max(np.abs(lse[b][:, rows[b]] - ref_lse[b][:, rows[b]])) < 1e-12
         assert np.all(np.isneginf(lse[b][:, ~rows[b]]))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_decode_window_is_the_full_window_oracle_on_the_whole_block(causal):
+    """Nq = Nk: the window decode equals the C oracle's sliding window (a
+    separately written mask) on full attention."""
+    B, H, N, d, W = 1, 2, 300, 8, 37
+    r = rng(17)
+    q, k, v = r.standard_normal((3, B, H, N, d))
+    o, lse = oracle.fwd_decode(q, k, v, 0.3, causal=causal, window_left=W)
+    o2, lse2 = oracle.fwd(q, k, v, 0.3, causal=causal, window_left=W)
+    assert np.max(np.abs(o - o2)) < 1e-12
+    assert np.max(np.abs(lse - lse2)) < 1e-12
+
+
+@pytest.mark.parametrize("Nq,L,W", [(1, 200, 0), (1, 200, 63), (4, 200, 10), (3, 5, 2)])
+def test_decode_window_identical_keys_closed_form(Nq, L, W):
+    """Identical keys: mean of V over j in [max(0, L - Nq + i - W), L - Nq + i]."""
+    Nk, d = 210, 5
+    r = rng(18)
+    q = r.standard_normal((1, 1, Nq, d))
+    k = np.broadcast_to(r.standard_normal(d), (1, 1, Nk, d)).copy()
+    v = r.standard_normal((1, 1, Nk, d))
+    o, lse = oracle.fwd_decode(q, k, v, 0.5, causal=True, seqlens_k=[L], window_left=W)
+    for i in range(Nq):
+        hi = L - Nq + i
+        lo = max(0, hi - W)
+        assert np.max(np.abs(o[0, 0, i] - v[0, 0, lo:hi + 1].mean(axis=0))) < 1e-12
+        assert abs(lse[0, 0, i] - (0.5 * q[0, 0, i] @ k[0, 0, 0] + np.log(hi - lo + 1))) < 1e-12
