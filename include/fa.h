@@ -187,7 +187,9 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  * row i of batch b sits at position L_b - Nq + i, where L_b = seqlens_k[b]
  * (clamped to [0, Nk]; Nk when seqlens_k is null). Without causal it sees
  * cache keys j < L_b; with causal, j <= L_b - Nq + i as well. A row that
- * sees no key gets O = 0 and lse = -inf.
+ * sees no key gets O = 0 and lse = -inf. window_left >= 0 adds a sliding window:
+ * row i sees only keys j >= L_b - Nq + i - window_left (cache tiles below every
+ * row's window are not read); -1 for none.
  *   q, o:          bf16 [B, H, Nq, d], contiguous, 16-byte aligned (device)
  *   k_cache, v_cache: bf16 [B, H_kv, Nk, d], contiguous, 16-byte aligned
  *   lse:           fp32 [B, H, Nq], natural log (device)
@@ -205,14 +207,15 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  *   head is cut, and then workspace may be NULL). The result does not depend
  *   on num_ctas beyond fp32 rounding of the merge.
  * Errors: FA_ERR_INVALID_ARG (null or unaligned pointers, sizes < 1, H not a
- * multiple of H_kv, scale not positive and finite, num_ctas < 0),
+ * multiple of H_kv, scale not positive and finite, num_ctas < 0,
+ * window_left < -1),
  * FA_ERR_UNSUPPORTED (d not 64/128, (H / H_kv) * Nq > 128, not an sm_100-family
  * GPU), FA_ERR_WORKSPACE, FA_ERR_CUDA. Asynchronous on `stream`; nothing is
  * allocated. */
 size_t fa_decode_workspace_size(int B, int H, int H_kv, int Nq, int Nk, int d, int num_ctas);
 fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                     int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
-                    const int32_t* seqlens_k, int num_ctas, void* workspace,
+                    int window_left, const int32_t* seqlens_k, int num_ctas, void* workspace,
                     size_t workspace_bytes, void* stream);
 
 /* FP8 forward with incoherent processing (FA-3's FP8 path, which the
@@ -285,10 +288,11 @@ fa_status fa_device_status(void* stream, int clear);
  * that runs out records FA_ERR_TIMEOUT and the kernel exits early. */
 void fa_set_wait_timeout_ns(uint64_t ns);
 
-/* Test hook for failure detection: mode 1 makes the next fa_fwd launch wait on
- * a barrier that nothing completes, so its bounded wait runs out and the
- * kernel returns with FA_ERR_TIMEOUT recorded. The hook is consumed by that
- * launch. mode 0 clears it. */
+/* Test hook for failure detection: mode 1 makes the next forward-type launch
+ * (fa_fwd and its _gqa / _window forms, fa_decode, fa_fwd_fp8) wait on a
+ * barrier that nothing completes, so its bounded wait runs out and the kernel
+ * returns with FA_ERR_TIMEOUT recorded. The hook is consumed by that launch.
+ * mode 0 clears it. */
 void fa_test_inject_stall(int mode);
 
 /* Static description of an error code. */

@@ -99,7 +99,7 @@ def load(build_if_missing: bool = False):
         lib.fa_bwd_noalloc.restype = i
         lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i, i]
         lib.fa_decode_workspace_size.restype = sz
-        lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
+        lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, i, vp, sz, vp]
         lib.fa_decode.restype = i
         lib.fa_fp8_workspace_size.argtypes = [i, i, i]
         lib.fa_fp8_workspace_size.restype = sz
@@ -285,13 +285,15 @@ def fa_decode_workspace_size(B, H, H_kv, Nq, Nk, d, num_ctas=0) -> int:
 
 
 def fa_decode(q, k_cache, v_cache, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal=False,
-              seqlens_k=None, num_ctas=0, workspace=None, workspace_bytes=0, stream=None) -> int:
+              seqlens_k=None, num_ctas=0, workspace=None, workspace_bytes=0, stream=None,
+              window_left=-1) -> int:
     if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda
                                   or not seqlens_k.is_contiguous()):
         raise ValueError("seqlens_k must be a contiguous int32 CUDA tensor")
     return load().fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, H, H_kv,
-                            Nq, Nk, d, float(scale), int(bool(causal)), _ptr(seqlens_k),
-                            int(num_ctas), _ptr(workspace), int(workspace_bytes), _stream(stream))
+                            Nq, Nk, d, float(scale), int(bool(causal)), int(window_left),
+                            _ptr(seqlens_k), int(num_ctas), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream))
 
 
 def fa_fp8_workspace_size(B, H, d) -> int:
@@ -407,7 +409,7 @@ def bwd(q, k, v, o, dout, lse, scale=None, causal=False, dropout_p=0.0, seed=0, 
 
 
 def decode(q, k_cache, v_cache, scale=None, causal=False, seqlens_k=None, num_ctas=0,
-           stream=None):
+           stream=None, window_left=-1):
     """Allocate O, lse (and the workspace, if the split needs one) with torch and
     run fa_decode: q [B, H, Nq, d] over k_cache, v_cache [B, H_kv, Nk, d].
     Returns (o, lse)."""
@@ -424,7 +426,7 @@ def decode(q, k_cache, v_cache, scale=None, causal=False, seqlens_k=None, num_ct
     ws_bytes = fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d, num_ctas)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
     _check(fa_decode(q, k_cache, v_cache, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, seqlens_k,
-                     num_ctas, ws, ws_bytes, stream), "fa_decode")
+                     num_ctas, ws, ws_bytes, stream, window_left), "fa_decode")
     return o, lse
 
 

@@ -481,11 +481,12 @@ size_t fa_decode_workspace_size(int B, int H, int H_kv, int Nq, int Nk, int d, i
 
 fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                     int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
-                    const int32_t* seqlens_k, int num_ctas, void* workspace,
+                    int window_left, const int32_t* seqlens_k, int num_ctas, void* workspace,
                     size_t workspace_bytes, void* stream) {
   DecodePlan p;
   fa_status st = decode_plan(B, H, H_kv, Nq, Nk, d, num_ctas, &p);
   if (st != FA_OK) return st;
+  if (window_left < -1) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
@@ -508,12 +509,13 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
   a.Nq = Nq;
   a.Nk = Nk;
   a.causal = causal ? 1 : 0;
+  a.wl = window_left;
   a.seqlens_k = seqlens_k;
   a.n_t = p.n_t;
   a.per_cta = p.per_cta;
   a.seg_max = p.seg_max;
   a.scale_log2 = scale * fa::kLog2e;
-  a.sync = make_sync(di, false);
+  a.sync = make_sync(di, true);
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   const size_t slots = static_cast<size_t>(B) * H * Nq * p.seg_max;
@@ -593,7 +595,7 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
     return FA_ERR_CUDA;
   fa::Fp8FwdArgs a;
   a.mask = make_mask(B, H, H, N, causal, nullptr, seqlens_k);
-  a.sync = make_sync(di, false);
+  a.sync = make_sync(di, true);
   a.scale_log2 = scale * fa::kLog2e;
   a.s_q = s_q;
   a.s_k = s_k;

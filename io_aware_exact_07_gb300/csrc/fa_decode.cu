@@ -54,8 +54,8 @@ struct DecL {
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // q_full, q_empty, k/v full/empty rings, s_full[3], s_free[3], p_full[3],
-  // o_full, o_free, drain, drain_pv
-  static constexpr int kNumBars = 2 + 4 * kDecMaxStages + 3 * kSBufs + 4;
+  // o_full, o_free, drain, drain_pv, stall
+  static constexpr int kNumBars = 2 + 4 * kDecMaxStages + 3 * kSBufs + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmemBytes <= 232448, "more shared memory than one CTA may hold");
@@ -68,7 +68,7 @@ struct DecBars {
   uint32_t k_full[kDecMaxStages], k_empty[kDecMaxStages];
   uint32_t v_full[kDecMaxStages], v_empty[kDecMaxStages];
   uint32_t s_full[kSBufs], s_free[kSBufs], p_full[kSBufs];
-  uint32_t o_full, o_free, drain, drain_pv;
+  uint32_t o_full, o_free, drain, drain_pv, stall;
 };
 
 // One piece of a CTA's run: key tiles [j0, j1) of K/V head bkv (j1 already
@@ -86,7 +86,8 @@ __device__ __forceinline__ int cache_len(const DecodeArgs& a, int b) {
 }
 
 // The piece that starts at flattened position pos of CTA cta's run, which
-// ends at hi; returns the position after it.
+// ends at hi; returns the position after it. Tiles below every row's sliding
+// window (row 0 of the group sees the lowest keys) are left out of it.
 __device__ __forceinline__ long long make_piece(const DecodeArgs& a, int cta, long long pos,
                                                 long long hi, Piece& p) {
   const int bkv = static_cast<int>(pos / a.n_t);
@@ -100,6 +101,11 @@ __device__ __forceinline__ long long make_piece(const DecodeArgs& a, int cta, lo
   p.j0 = static_cast<int>(pos - head0);
   p.j1 = static_cast<int>(end - head0);
   if (p.j1 > n_valid) p.j1 = n_valid;
+  if (a.wl >= 0) {
+    const int lo = L - a.Nq - a.wl;  // lowest key any row of the group sees
+    const int jlo = lo > 0 ? lo / kTile : 0;
+    if (p.j0 < jlo) p.j0 = jlo;
+  }
   if (p.j1 < p.j0) p.j1 = p.j0;
   p.seg = cta - c0;
   p.n_seg = c1 - c0 + 1;
@@ -148,6 +154,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     bars.o_free = nb();
     bars.drain = nb();
     bars.drain_pv = nb();
+    bars.stall = nb();
   }
   if (tid == 0) {
     *abort_flag = 0;
@@ -168,6 +175,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_init(bars.o_free, 32 * n_sw);
     mbar_init(bars.drain, 1);
     mbar_init(bars.drain_pv, 1);
+    mbar_init(bars.stall, 1);
     fence_mbar_init();
   }
   if (warp == kDecMmaWarp) {
@@ -254,6 +262,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
       uint32_t it = 0;
       bool ok = true;
+      // Test hook: a barrier that nothing completes, so the bounded wait runs out.
+      if (args.sync.inject_stall && !mbar_wait(bars.stall, 0, tmo, abort_flag)) ok = false;
       int np = 0;
       for (long long pos = lo; pos < hi && ok; ++np) {
         Piece pc;
@@ -357,11 +367,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       Piece pc;
       pos = make_piece(args, blockIdx.x, pos, hi, pc);
       const int Lb = cache_len(args, pc.bkv / args.Hkv);
-      int vis = Lb;  // keys [0, vis) are visible to this row
+      int vis = Lb;  // keys [key_lo, vis) are visible to this row
       if (args.causal) {
         const int lc = Lb - args.Nq + i + 1;
         vis = lc < vis ? lc : vis;
       }
+      const int key_lo = args.wl >= 0 ? Lb - args.Nq + i - args.wl : 0;
       float m_ref = -INFINITY;  // reference maximum, scaled log2 units
       float l_sum = 0.f;        // running sum of exp2(s*c - m_ref)
       for (int j = pc.j0; j < pc.j1; ++j) {
@@ -380,11 +391,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         float s[128];
 #pragma unroll
         for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(sr[k]);
-        const int lim = vis - j * kTile;  // keys [0, lim) of this tile are visible
-        if (lim < kTile) {
+        const int lim = vis - j * kTile;     // keys [lo, lim) of this tile are visible
+        const int lo = key_lo - j * kTile;
+        if (lim < kTile || lo > 0) {
 #pragma unroll
           for (int k = 0; k < 128; ++k)
-            if (k >= lim) s[k] = -INFINITY;
+            if (k >= lim || k < lo) s[k] = -INFINITY;
         }
         float mx[8];
 #pragma unroll

@@ -49,8 +49,8 @@ struct F8L {
   static constexpr int kPOff = kVOff + kStages * kTileBytes;  // P_a, P_b
   static constexpr int kBarOff = kPOff + 2 * kTileBytes;
   // q_full[2], q_empty, k_full/k_empty/v_full/v_empty[S], s_full[2], s_free[2],
-  // p_full[2], pv_done[2], o_free[2], drain, drain2
-  static constexpr int kNumBars = 3 + 4 * kStages + 10 + 2;
+  // p_full[2], pv_done[2], o_free[2], drain, drain2, stall
+  static constexpr int kNumBars = 3 + 4 * kStages + 10 + 3;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
   static_assert(kSmemBytes <= 232448, "more shared memory than one CTA may hold");
@@ -63,7 +63,7 @@ struct F8Bars {
   uint32_t k_full[F8L::kStages], k_empty[F8L::kStages], v_full[F8L::kStages],
       v_empty[F8L::kStages];
   uint32_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
-  uint32_t drain, drain2;
+  uint32_t drain, drain2, stall;
 };
 
 struct F8Unit {
@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     for (int x = 0; x < 2; ++x) bars.o_free[x] = nb();
     bars.drain = nb();
     bars.drain2 = nb();
+    bars.stall = nb();
   }
   if (tid == 0) {
     *abort_flag = 0;
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     }
     mbar_init(bars.drain, 1);
     mbar_init(bars.drain2, 1);
+    mbar_init(bars.stall, 1);
     fence_mbar_init();
   }
   if (warp == kF8MmaWarp) {
@@ -255,6 +257,14 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint32_t it = 0, sf_cnt0 = 0, sf_cnt1 = 0;
     bool s_seen0 = false, s_seen1 = false;
     bool ok = true;
+    if (args.sync.inject_stall && leader) {
+      // Test hook: a barrier that nothing completes, so the bounded wait runs out.
+      if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
+        fail();
+        ok = false;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
     auto issue_S = [&](int x, int s) {
       const uint64_t dq = x ? dQb : dQa;
       const uint64_t dk = dK0 + static_cast<uint64_t>(s) * kStep;

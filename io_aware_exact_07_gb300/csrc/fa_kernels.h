@@ -41,6 +41,7 @@ struct BwdArgs {
 struct DecodeArgs {
   int B, H, Hkv, Nq, Nk;        // query heads H share Hkv K/V heads; Nq query rows, Nk cache rows
   int causal;                   // query row i sits at position L_b - Nq + i
+  int wl;                       // sliding window: keys >= L_b - Nq + i - wl only (-1: none)
   const int32_t* seqlens_k;     // [B] valid cache lengths L_b, or null (= Nk)
   int n_t;                      // ceil(Nk / 128): key tiles per K/V head
   int per_cta;                  // (K/V head, key tile) pairs per CTA

@@ -13,20 +13,20 @@ from _parity import LSE_TOL, o_within_tol
 pytestmark = pytest.mark.gpu
 
 
-def run(B, H, Hkv, Nq, Nk, d, causal=False, lengths=None, num_ctas=0, seed=0):
+def run(B, H, Hkv, Nq, Nk, d, causal=False, lengths=None, num_ctas=0, seed=0, window_left=-1):
     w = inputs.DecodeWorkload("t", B, H, Hkv, Nq, Nk, d, causal=causal, lengths=lengths,
                               seed=seed)
     x = inputs.draw_decode(w)
     sl = None if x["seqlens"] is None else x["seqlens"].cuda()
     o, lse = fa.decode(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), w.scale, causal=causal,
-                       seqlens_k=sl, num_ctas=num_ctas)
+                       seqlens_k=sl, num_ctas=num_ctas, window_left=window_left)
     torch.cuda.synchronize()
     assert fa.fa_device_status() == fa.FA_OK
     f64 = lambda t: t.double().numpy()
     o_ref, lse_ref = oracle.fwd_decode(f64(x["q"]), f64(x["k"]), f64(x["v"]), w.scale,
                                        causal=causal,
                                        seqlens_k=None if x["seqlens"] is None
-                                       else x["seqlens"].numpy())
+                                       else x["seqlens"].numpy(), window_left=window_left)
     check(o, lse, o_ref, lse_ref)
     return o, lse
 
@@ -119,3 +119,15 @@ def test_decode_rejects_bad_arguments():
         fa.FA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert fa.fa_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("B,H,Hkv,Nq,Nk,d,causal,lengths,wl,ctas", [
+    (2, 8, 2, 1, 5000, 128, True, None, 0, 0),           # a window of one key
+    (2, 8, 2, 4, 5000, 64, True, (100, 5000), 300, 0),   # ragged caches, 301-key window
+    (1, 4, 1, 16, 3000, 128, False, None, 1000, 7),      # non-causal, heads cut over 7 CTAs
+    (2, 4, 4, 1, 4100, 128, True, None, 127, 1000),      # window on a tile edge, one tile per CTA
+    (1, 2, 2, 64, 2000, 64, True, None, 4095, 0),        # window wider than the cache
+])
+def test_decode_sliding_window(B, H, Hkv, Nq, Nk, d, causal, lengths, wl, ctas):
+    run(B, H, Hkv, Nq, Nk, d, causal, lengths, num_ctas=ctas, seed=wl + Nk, window_left=wl)
+
