@@ -236,12 +236,12 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
  * fa_fwd_fp8: attention of Q^ = dec(q8) s_q, K^ = dec(k8) s_k, V^ = dec(vt8)^T s_v
  *   (rotated Q and K give the same scores), both products on the tensor core
  *   in FP8 with fp32 accumulation; P is rounded to e4m3 for the PV product
- *   (kept between 2^7 and 2^8 at each row's maximum, so weights down to 2^-16
+ *   (kept between 2^5 and 2^8 at each row's maximum, so weights down to 2^-14
  *   of it are represented). Causal and key padding as fa_fwd. o: bf16
  *   [B, H, N, 128]; lse: fp32 [B, H, N] (natural log).
  * Accuracy contract (the exactness of fa_fwd does not carry over): against
  * exact attention of the dequantised inputs, |O - O^| <= 2^-4 sum_j P_ij |v^_j|
- * + 2^-17 sum_j |v^_j| (the e4m3 rounding of P, with underflow below 2^-9)
+ * + 2^-15 sum_j |v^_j| (the e4m3 rounding of P, with underflow below 2^-9)
  * + 1.5 bf16 half-ulps of O; lse within 1e-3. Against the bf16 inputs the
  * error adds the quantisation of Q, K, V, which the rotation reduces when
  * channels carry outliers.

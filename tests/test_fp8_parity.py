@@ -54,11 +54,13 @@ def test_quantiser_matches_oracle(N, rot):
 
 
 def fp8_contract(o, lse, o_ref, lse_ref, o_abs, vsum_abs):
-    """|O - O^| <= 2^-4 sum P|v^| + 2^-17 sum |v^| + 1.5 bf16 half-ulps; lse 1e-3."""
+    """|O - O^| <= 2^-4 sum P|v^| + 2^-15 sum |v^| + 1.5 bf16 half-ulps; lse 1e-3. The
+    second term: P's e4m3 rounding is absolute (at most 2^-10, half the smallest
+    subnormal) below 2^-6, relative to a row maximum of at least 2^5."""
     o = o.float().cpu().numpy().astype(np.float64)
     mag = np.maximum(np.abs(o_ref), 1e-30)
     half_ulp = np.exp2(np.floor(np.log2(mag)) - 8.0)
-    tol = 2.0 ** -4 * o_abs + 2.0 ** -17 * vsum_abs + 1.5 * half_ulp + 1e-6
+    tol = 2.0 ** -4 * o_abs + 2.0 ** -15 * vsum_abs + 1.5 * half_ulp + 1e-6
     excess = np.abs(o - o_ref) - tol
     assert excess.max() <= 0, f"FP8 contract exceeded by {excess.max()}"
     assert lse_err(lse.cpu().numpy(), lse_ref) <= LSE_TOL
