@@ -52,6 +52,8 @@ def check(o, lse, o_ref, lse_ref):
     (1, 128, 1, 1, 777, 64, False, None),        # 128 query heads over one K/V head
     (4, 16, 16, 1, 128, 64, False, None),        # one key tile per head
     (1, 8, 1, 16, 2048, 128, True, (10, 2048)),  # 8 x 16 = 128 rows: a full query tile
+    (3, 2, 2, 1, 1, 64, False, None),             # a one-key cache
+    (2, 2, 1, 5, 1, 128, True, None),             # one key, more query rows than keys
 ])
 def test_decode_matches_oracle(B, H, Hkv, Nq, Nk, d, causal, lengths):
     run(B, H, Hkv, Nq, Nk, d, causal, lengths, seed=B + Nk)

@@ -68,7 +68,9 @@ def fp8_contract(o, lse, o_ref, lse_ref, o_abs, vsum_abs):
 
 
 @pytest.mark.parametrize("N,causal,padding", [(256, False, None), (1000, True, None),
-                                              (777, False, (100, 777)), (2048, True, (900, 2048))])
+                                              (777, False, (100, 777)), (2048, True, (900, 2048)),
+                                              (1, False, None), (17, True, None),
+                                              (300, False, (0, 40))])
 def test_fp8_forward_within_contract(N, causal, padding):
     B, H, d = 2, 2, 128
     x = inputs.draw_fp8_codes(B, H, N, d, seed=N)
