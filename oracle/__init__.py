@@ -376,8 +376,9 @@ def quantize_fp8(q, k, v, signs):
 def fwd_fp8(q8, k8, v8, s_q, s_k, s_v, scale, causal=False, seqlens_k=None):
     """Exact attention (the forward above, fp64) of the dequantised inputs
     Q^ = dec(q8) s_q, K^ = dec(k8) s_k, V^ = dec(v8) s_v: what the FP8 kernel
-    computes before its own rounding of P. q8, k8, v8: uint8 [B, H, N, d]."""
+    computes before its own rounding of P. q8: uint8 [B, H, N, d]; k8, v8: uint8
+    [B, Hkv, N, d] with Hkv dividing H (grouped K/V heads as in fwd_gqa)."""
     qh = e4m3_decode(q8) * np.asarray(s_q, dtype=np.float64)[:, :, None, None]
     kh = e4m3_decode(k8) * np.asarray(s_k, dtype=np.float64)[:, :, None, None]
     vh = e4m3_decode(v8) * np.asarray(s_v, dtype=np.float64)[:, :, None, :]
-    return fwd(qh, kh, vh, scale, causal=causal, seqlens_k=seqlens_k)
+    return fwd_gqa(qh, kh, vh, scale, causal=causal, seqlens_k=seqlens_k)

@@ -127,3 +127,37 @@ def test_no_rotation_quantises_the_inputs_themselves():
     assert np.array_equal(q8, oracle.e4m3_encode(q / sq[:, :, None, None]))
     assert np.array_equal(k8, oracle.e4m3_encode(k / sk[:, :, None, None]))
     assert np.allclose(sq, np.abs(q).max(axis=(2, 3)) / 448.0, rtol=1e-15)
+
+
+def test_fp8_forward_grouped_heads_is_the_grouped_plain_forward():
+    """Grouped K/V heads: the FP8 oracle on Hkv K/V heads is, per query head
+    h, the plain fp64 forward of that head against K/V head h // (H / Hkv),
+    written here head by head (not through the repeat in fwd_gqa)."""
+    r = rng(35)
+    B, H, Hkv, N, d = 2, 6, 2, 90, 16
+    q8 = r.integers(0, 256, (B, H, N, d)).astype(np.uint8)
+    k8, v8 = (r.integers(0, 256, (B, Hkv, N, d)).astype(np.uint8) for _ in range(2))
+    for c in (q8, k8, v8):
+        c[(c & 0x7F) == 0x7F] = 0  # no NaN codes
+    sq = r.uniform(0.001, 0.01, (B, H))
+    sk = r.uniform(0.001, 0.01, (B, Hkv))
+    sv = r.uniform(0.001, 0.01, (B, Hkv, d))
+    sl = np.array([90, 41])
+    o, lse = oracle.fwd_fp8(q8, k8, v8, sq, sk, sv, 0.3, causal=True, seqlens_k=sl)
+    G = H // Hkv
+    for b in range(B):
+        for h in range(H):
+            j = h // G
+            qh = oracle.e4m3_decode(q8[b, h]) * sq[b, h]
+            kh = oracle.e4m3_decode(k8[b, j]) * sk[b, j]
+            vh = oracle.e4m3_decode(v8[b, j]) * sv[b, j][None, :]
+            o1, l1 = oracle.fwd(qh[None, None], kh[None, None], vh[None, None], 0.3, causal=True,
+                                seqlens_k=sl[b:b + 1])
+            assert np.array_equal(o[b, h], o1[0, 0]) and np.array_equal(lse[b, h], l1[0, 0])
+    # the quantiser's K/V scales are per K/V head: a K/V head with 10x the values
+    # gets 10x the scale and the same codes
+    x = r.standard_normal((1, 1, 40, 16))
+    y = np.concatenate([x, 10 * x], axis=1)
+    _, k8q, v8q, _, skq, svq = oracle.quantize_fp8(np.zeros((1, 4, 40, 16)), y, y, None)
+    assert np.allclose(skq[0, 1], 10 * skq[0, 0], rtol=1e-14) and np.array_equal(k8q[0, 0], k8q[0, 1])
+    assert np.allclose(svq[0, 1], 10 * svq[0, 0], rtol=1e-14) and np.array_equal(v8q[0, 0], v8q[0, 1])
