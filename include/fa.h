@@ -257,6 +257,22 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
                      const float* s_k, const float* s_v, void* o, float* lse, int B, int H, int N,
                      int d, float scale, int causal, const int32_t* seqlens_k, void* stream);
 
+/* Grouped K/V heads (H_kv dividing H; query head h of batch b uses K/V head
+ * b H_kv + h / (H / H_kv), as fa_fwd_gqa): the same two calls with k, v, k8
+ * shaped [B, H_kv, N, 128], vt8 [B, H_kv, 128, Np], s_k [B, H_kv] and s_v
+ * [B, H_kv, 128]; q, q8, s_q, o and lse keep H. The workspace of
+ * fa_fp8_workspace_size(B, H, 128) bytes also covers this case. fa_fp8_quantize
+ * and fa_fwd_fp8 are these with H_kv = H. FA_ERR_INVALID_ARG also when H_kv < 1
+ * or H is not a multiple of H_kv. */
+fa_status fa_fp8_quantize_gqa(const void* q, const void* k, const void* v, const float* signs,
+                              int B, int H, int H_kv, int N, int d, void* q8, void* k8, void* vt8,
+                              float* s_q, float* s_k, float* s_v, void* workspace,
+                              size_t workspace_bytes, void* stream);
+fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* vt8, const float* s_q,
+                         const float* s_k, const float* s_v, void* o, float* lse, int B, int H,
+                         int H_kv, int N, int d, float scale, int causal,
+                         const int32_t* seqlens_k, void* stream);
+
 /* Quantised dropout threshold round(256 p) used by fa_fwd / fa_bwd (-1 if p is
  * outside [0, 1)). The effective dropout rate is fa_dropout_p8(p) / 256. */
 int fa_dropout_p8(float dropout_p);
@@ -289,7 +305,8 @@ fa_status fa_device_status(void* stream, int clear);
 void fa_set_wait_timeout_ns(uint64_t ns);
 
 /* Test hook for failure detection: mode 1 makes the next forward-type launch
- * (fa_fwd and its _gqa / _window forms, fa_decode, fa_fwd_fp8) wait on a
+ * (fa_fwd and its _gqa / _window forms, fa_decode, fa_fwd_fp8 and
+ * fa_fwd_fp8_gqa) wait on a
  * barrier that nothing completes, so its bounded wait runs out and the kernel
  * returns with FA_ERR_TIMEOUT recorded. The hook is consumed by that launch.
  * mode 0 clears it. */

@@ -36,6 +36,7 @@ EXPORTS = (
     "fa_bwd_workspace_size", "fa_bwd_preprocess",
     "fa_bwd_dkdv", "fa_bwd_dq", "fa_decode", "fa_decode_workspace_size",
     "fa_fp8_workspace_size", "fa_fp8_vt_stride", "fa_fp8_quantize", "fa_fwd_fp8",
+    "fa_fp8_quantize_gqa", "fa_fwd_fp8_gqa",
     "fa_bwd_noalloc", "fa_dropout_p8", "fa_debug_dropout_keep",
     "fa_debug_philox", "fa_butterfly_mask", "fa_device_status", "fa_set_wait_timeout_ns",
     "fa_test_inject_stall", "fa_status_string",
@@ -110,6 +111,11 @@ def load(build_if_missing: bool = False):
         lib.fa_fp8_quantize.restype = i
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp]
         lib.fa_fwd_fp8.restype = i
+        lib.fa_fp8_quantize_gqa.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, vp, vp,
+                                            vp, sz, vp]
+        lib.fa_fp8_quantize_gqa.restype = i
+        lib.fa_fwd_fp8_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp]
+        lib.fa_fwd_fp8_gqa.restype = i
         lib.fa_dropout_p8.argtypes = [f]
         lib.fa_dropout_p8.restype = i
         lib.fa_debug_dropout_keep.argtypes = [vp, i, i, i, f, u64, u64, vp]
@@ -319,6 +325,22 @@ def fa_fwd_fp8(q8, k8, vt8, s_q, s_k, s_v, o, lse, B, H, N, d, scale, causal=Fal
                              _stream(stream))
 
 
+def fa_fp8_quantize_gqa(q, k, v, signs, B, H, Hkv, N, d, q8, k8, vt8, s_q, s_k, s_v, workspace,
+                        workspace_bytes, stream=None) -> int:
+    return load().fa_fp8_quantize_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(signs), B, H, Hkv, N, d,
+                                      _ptr(q8), _ptr(k8), _ptr(vt8), _ptr(s_q), _ptr(s_k),
+                                      _ptr(s_v), _ptr(workspace), int(workspace_bytes),
+                                      _stream(stream))
+
+
+def fa_fwd_fp8_gqa(q8, k8, vt8, s_q, s_k, s_v, o, lse, B, H, Hkv, N, d, scale, causal=False,
+                   seqlens_k=None, stream=None) -> int:
+    _, sl = _opt_ptrs(None, seqlens_k)
+    return load().fa_fwd_fp8_gqa(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(s_q), _ptr(s_k), _ptr(s_v),
+                                 _ptr(o), _ptr(lse), B, H, Hkv, N, d, float(scale),
+                                 int(bool(causal)), sl, _stream(stream))
+
+
 def fa_dropout_p8(p: float) -> int:
     return int(load().fa_dropout_p8(float(p)))
 
@@ -431,30 +453,43 @@ def decode(q, k_cache, v_cache, scale=None, causal=False, seqlens_k=None, num_ct
 
 
 def fp8_quantize(q, k, v, signs=None, stream=None):
-    """Allocate the e4m3 tensors and scales with torch and run fa_fp8_quantize.
+    """Allocate the e4m3 tensors and scales with torch and run fa_fp8_quantize
+    (fa_fp8_quantize_gqa when k and v have fewer heads than q).
     Returns dict(q8, k8, vt8, s_q, s_k, s_v) (uint8 codes, fp32 scales)."""
     _check_qkv(q, k, v)
+    Hkv = _kv_heads(q, k, v)
     B, H, N, d = q.shape
     dev = q.device
     Np = fa_fp8_vt_stride(N)
     out = dict(q8=torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
-               k8=torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
-               vt8=torch.empty((B, H, d, Np), dtype=torch.uint8, device=dev),
+               k8=torch.empty((B, Hkv, N, d), dtype=torch.uint8, device=dev),
+               vt8=torch.empty((B, Hkv, d, Np), dtype=torch.uint8, device=dev),
                s_q=torch.empty((B, H), dtype=torch.float32, device=dev),
-               s_k=torch.empty((B, H), dtype=torch.float32, device=dev),
-               s_v=torch.empty((B, H, d), dtype=torch.float32, device=dev))
+               s_k=torch.empty((B, Hkv), dtype=torch.float32, device=dev),
+               s_v=torch.empty((B, Hkv, d), dtype=torch.float32, device=dev))
     wsb = fa_fp8_workspace_size(B, H, d)
     ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
-    _check(fa_fp8_quantize(q, k, v, signs, B, H, N, d, out["q8"], out["k8"], out["vt8"],
-                           out["s_q"], out["s_k"], out["s_v"], ws, wsb, stream), "fa_fp8_quantize")
+    if Hkv == H:
+        st = fa_fp8_quantize(q, k, v, signs, B, H, N, d, out["q8"], out["k8"], out["vt8"],
+                             out["s_q"], out["s_k"], out["s_v"], ws, wsb, stream)
+    else:
+        st = fa_fp8_quantize_gqa(q, k, v, signs, B, H, Hkv, N, d, out["q8"], out["k8"],
+                                 out["vt8"], out["s_q"], out["s_k"], out["s_v"], ws, wsb, stream)
+    _check(st, "fa_fp8_quantize")
     return out
 
 
 def fwd_fp8(qz, scale, causal=False, seqlens_k=None, stream=None):
-    """Run fa_fwd_fp8 on the output of fp8_quantize; returns (o bf16, lse)."""
+    """Run fa_fwd_fp8 (fa_fwd_fp8_gqa with grouped K/V heads) on the output of
+    fp8_quantize; returns (o bf16, lse)."""
     B, H, N, d = qz["q8"].shape
+    Hkv = qz["k8"].shape[1]
     o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=qz["q8"].device)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=qz["q8"].device)
-    _check(fa_fwd_fp8(qz["q8"], qz["k8"], qz["vt8"], qz["s_q"], qz["s_k"], qz["s_v"], o, lse, B, H,
-                      N, d, scale, causal, seqlens_k, stream), "fa_fwd_fp8")
+    args = (qz["q8"], qz["k8"], qz["vt8"], qz["s_q"], qz["s_k"], qz["s_v"], o, lse)
+    if Hkv == H:
+        st = fa_fwd_fp8(*args, B, H, N, d, scale, causal, seqlens_k, stream)
+    else:
+        st = fa_fwd_fp8_gqa(*args, B, H, Hkv, N, d, scale, causal, seqlens_k, stream)
+    _check(st, "fa_fwd_fp8")
     return o, lse

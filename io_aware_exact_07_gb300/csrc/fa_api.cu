@@ -530,17 +530,18 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
 }
 
 size_t fa_fp8_workspace_size(int B, int H, int d) {
+  // B*H amaxes of Q, and of K plus 128 columns of V per K/V head: at most 130 B*H
   if (B < 1 || H < 1 || d != 128) return 0;
   return round256(static_cast<size_t>(B) * H * (2 + 128) * sizeof(unsigned int));
 }
 
 int fa_fp8_vt_stride(int N) { return N < 1 ? 0 : (N + 15) / 16 * 16; }
 
-fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs, int B,
-                          int H, int N, int d, void* q8, void* k8, void* vt8, float* s_q,
-                          float* s_k, float* s_v, void* workspace, size_t workspace_bytes,
-                          void* stream) {
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+fa_status fa_fp8_quantize_gqa(const void* q, const void* k, const void* v, const float* signs,
+                              int B, int H, int Hkv, int N, int d, void* q8, void* k8, void* vt8,
+                              float* s_q, float* s_k, float* s_v, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (B < 1 || H < 1 || N < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H * N >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   if (d != 128) return FA_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k, v, q8, k8, vt8, s_q, s_k, s_v};  // signs may be null
@@ -562,6 +563,7 @@ fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const flo
   a.signs = signs;
   a.B = B;
   a.H = H;
+  a.Hkv = Hkv;
   a.N = N;
   a.Np = fa_fp8_vt_stride(N);
   a.amax = static_cast<unsigned int*>(workspace);
@@ -576,10 +578,11 @@ fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const flo
              : FA_ERR_CUDA;
 }
 
-fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s_q,
-                     const float* s_k, const float* s_v, void* o, float* lse, int B, int H, int N,
-                     int d, float scale, int causal, const int32_t* seqlens_k, void* stream) {
-  fa_status st = check_common(B, H, N, d, scale, 0.f, H);
+fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* vt8, const float* s_q,
+                         const float* s_k, const float* s_v, void* o, float* lse, int B, int H,
+                         int Hkv, int N, int d, float scale, int causal, const int32_t* seqlens_k,
+                         void* stream) {
+  fa_status st = check_common(B, H, N, d, scale, 0.f, Hkv);
   if (st != FA_OK) return st;
   if (d != 128) return FA_ERR_UNSUPPORTED;
   if (!q8 || !k8 || !vt8 || !s_q || !s_k || !s_v || !o || !lse) return FA_ERR_INVALID_ARG;
@@ -590,11 +593,12 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
   if ((st = device_info(&di)) != FA_OK) return st;
   const int Np = fa_fp8_vt_stride(N);
   CUtensorMap tq, tk, tv;
-  if (!encode_map_u8(&tq, q8, B * H, N, 128, 128) || !encode_map_u8(&tk, k8, B * H, N, 128, 128) ||
-      !encode_map_u8(&tv, vt8, B * H, 128, Np, Np))
+  if (!encode_map_u8(&tq, q8, B * H, N, 128, 128) ||
+      !encode_map_u8(&tk, k8, B * Hkv, N, 128, 128) ||
+      !encode_map_u8(&tv, vt8, B * Hkv, 128, Np, Np))
     return FA_ERR_CUDA;
   fa::Fp8FwdArgs a;
-  a.mask = make_mask(B, H, H, N, causal, nullptr, seqlens_k);
+  a.mask = make_mask(B, H, Hkv, N, causal, nullptr, seqlens_k);
   a.sync = make_sync(di, true);
   a.scale_log2 = scale * fa::kLog2e;
   a.s_q = s_q;
@@ -606,6 +610,21 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
                  cudaSuccess
              ? FA_OK
              : FA_ERR_CUDA;
+}
+
+fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs, int B,
+                          int H, int N, int d, void* q8, void* k8, void* vt8, float* s_q,
+                          float* s_k, float* s_v, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  return fa_fp8_quantize_gqa(q, k, v, signs, B, H, H, N, d, q8, k8, vt8, s_q, s_k, s_v, workspace,
+                             workspace_bytes, stream);
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* s_q,
+                     const float* s_k, const float* s_v, void* o, float* lse, int B, int H, int N,
+                     int d, float scale, int causal, const int32_t* seqlens_k, void* stream) {
+  return fa_fwd_fp8_gqa(q8, k8, vt8, s_q, s_k, s_v, o, lse, B, H, H, N, d, scale, causal,
+                        seqlens_k, stream);
 }
 
 int fa_dropout_p8(float dropout_p) { return p8_of(dropout_p); }

@@ -22,6 +22,8 @@
 //    (a tighter reference, 1 with offset 7, rescales O more often for 3 %);
 //  - the scales: S is multiplied by s_q s_k (folded into the exponent's
 //    factor) and O's column c by s_v[c] in the epilogue.
+//  - grouped K/V heads (Hkv dividing H): query head h of batch b reads K/V
+//    tiles and scales of K/V head b Hkv + h / (H / Hkv).
 // Tensor memory: S_a, S_b, O_a, O_b (128 columns each).
 #include <cuda.h>
 #include <cuda_fp8.h>
@@ -68,16 +70,19 @@ struct F8Bars {
 };
 
 struct F8Unit {
-  int bh, b, qt0;
+  int bh, bhk, b, qt0;  // query head, its K/V head, batch row, first query tile
 };
 
-__device__ __forceinline__ F8Unit f8_unit(int u, int H, int n_qblk, int causal) {
+// Units run head by head, so the query heads of one K/V group are neighbours
+// in the schedule and their K/V tiles are read from L2 after the first.
+__device__ __forceinline__ F8Unit f8_unit(int u, const MaskParams& m, int n_qblk) {
   F8Unit c;
   const int bh = u / n_qblk;
   int qb = u % n_qblk;
-  if (causal) qb = n_qblk - 1 - qb;  // longest causal units of a head first
+  if (m.causal) qb = n_qblk - 1 - qb;  // longest causal units of a head first
   c.bh = bh;
-  c.b = bh / H;
+  c.bhk = kv_head(m, bh);
+  c.b = bh / m.H;
   c.qt0 = 2 * qb;
   return c;
 }
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     }
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const F8Unit uc = f8_unit(u, mk.H, n_qblk, mk.causal);
+      const F8Unit uc = f8_unit(u, mk, n_qblk);
       const int kv_len = kv_len_of(mk, uc.b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       int jmax = n_kv;
@@ -220,7 +225,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           }
           if (lane == 0) {
             mbar_expect_tx(bars.k_full[s], L::kTileBytes);
-            tma_load_3d(sK + s * L::kTileBytes, &tm_k, 0, j * kTile, uc.bh, bars.k_full[s]);
+            tma_load_3d(sK + s * L::kTileBytes, &tm_k, 0, j * kTile, uc.bhk, bars.k_full[s]);
           }
           ++k_arms;
           if (!mbar_wait_warp(bars.v_empty[s], ph ^ 1u, tmo, abort_flag)) {
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           if (lane == 0) {
             mbar_expect_tx(bars.v_full[s], L::kTileBytes);
             // V^T: keys j*128 .. j*128+127 (innermost), all 128 channels
-            tma_load_3d(sV + s * L::kTileBytes, &tm_vt, j * kTile, 0, uc.bh, bars.v_full[s]);
+            tma_load_3d(sV + s * L::kTileBytes, &tm_vt, j * kTile, 0, uc.bhk, bars.v_full[s]);
           }
           ++v_arms;
           ++it;
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     };
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const F8Unit uc = f8_unit(u, mk.H, n_qblk, mk.causal);
+      const F8Unit uc = f8_unit(u, mk, n_qblk);
       const int kv_len = kv_len_of(mk, uc.b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       int jmax = n_kv;
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const F8Unit uc = f8_unit(u, mk.H, n_qblk, mk.causal);
+      const F8Unit uc = f8_unit(u, mk, n_qblk);
       const int kv_len = kv_len_of(mk, uc.b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
       int jmax = n_kv;
@@ -422,7 +427,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const F8Unit uc = f8_unit(u, mk.H, n_qblk, mk.causal);
+      const F8Unit uc = f8_unit(u, mk, n_qblk);
       const int qt = uc.qt0 + x;
       const int row = qt * kTile + t;
       const int kv_len = kv_len_of(mk, uc.b);
@@ -430,7 +435,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       int jmax = n_kv;
       if (mk.causal && qt + 1 < jmax) jmax = qt + 1;
       // S of the stored codes times s_q s_k is the score; c folds both into the exponent
-      const float c_log2 = args.scale_log2 * args.s_q[uc.bh] * args.s_k[uc.bh];
+      const float c_log2 = args.scale_log2 * args.s_q[uc.bh] * args.s_k[uc.bhk];
       const uint64_t c2 = f2_pack(c_log2, c_log2);
       float m_ref = -INFINITY;
       float l_sum = 0.f;
@@ -552,7 +557,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       tc_fence_after();
       const bool row_ok = row < N;
       const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
-      const float* sv = args.s_v + static_cast<size_t>(uc.bh) * 128;
+      const float* sv = args.s_v + static_cast<size_t>(uc.bhk) * 128;
       __nv_bfloat16* orow = args.o + (static_cast<size_t>(uc.bh) * N + static_cast<size_t>(row)) * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {

@@ -60,14 +60,17 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, int d, cudaStream_t strea
 
 // FP8 forward (fa_fp8.cu, fa_fwd_fp8.cu), head dimension 128.
 struct Fp8QuantArgs {
-  const __nv_bfloat16 *q, *k, *v;  // [B, H, N, 128]
+  const __nv_bfloat16* q;          // [B, H, N, 128]
+  const __nv_bfloat16 *k, *v;      // [B, Hkv, N, 128]
   const float* signs;              // [128], +-1: the rotation's random signs
-  int B, H, N, Np;                 // Np: row stride of vt8, N rounded up to 16
-  unsigned int* amax;              // workspace [B*H*130]
-  uint8_t *q8, *k8;                // e4m3 [B, H, N, 128] (rotated, scaled)
-  uint8_t* vt8;                    // e4m3 [B, H, 128, Np] (V transposed, scaled per column)
-  float *s_q, *s_k;                // [B*H]
-  float* s_v;                      // [B*H, 128]
+  int B, H, Hkv, N, Np;            // Np: row stride of vt8, N rounded up to 16
+  unsigned int* amax;              // workspace [B*H + 129*B*Hkv]
+  uint8_t* q8;                     // e4m3 [B, H, N, 128] (rotated, scaled)
+  uint8_t* k8;                     // e4m3 [B, Hkv, N, 128] (rotated, scaled)
+  uint8_t* vt8;                    // e4m3 [B, Hkv, 128, Np] (V transposed, scaled per column)
+  float* s_q;                      // [B*H]
+  float* s_k;                      // [B*Hkv]
+  float* s_v;                      // [B*Hkv, 128]
 };
 
 struct Fp8FwdArgs {

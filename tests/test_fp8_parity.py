@@ -24,11 +24,12 @@ def e4m3_gap(y):
     return mags[idx] - mags[np.maximum(idx - 1, 0)]
 
 
-@pytest.mark.parametrize("N,rot", [(300, True), (1000, True), (129, False)])
-def test_quantiser_matches_oracle(N, rot):
-    B, H, d = 2, 3, 128
+@pytest.mark.parametrize("N,rot,Hkv", [(300, True, 3), (1000, True, 3), (129, False, 3),
+                                       (300, True, 1), (520, False, 2)])
+def test_quantiser_matches_oracle(N, rot, Hkv):
+    B, H, d = 2, 3 if Hkv != 2 else 4, 128
     x = inputs.draw_small(B, H, N, d, seed=N, with_grad=False)
-    q, k, v = x["q"], x["k"], x["v"]
+    q, k, v = x["q"], x["k"][:, :Hkv].contiguous(), x["v"][:, :Hkv].contiguous()
     k[..., 5] *= 30  # an outlier channel
     signs = inputs.rotation_signs(d, seed=1)
     z = fa.fp8_quantize(q.cuda(), k.cuda(), v.cuda(), signs.cuda() if rot else None)
@@ -40,7 +41,7 @@ def test_quantiser_matches_oracle(N, rot):
         assert np.allclose(z[name].cpu().numpy(), ref, rtol=2e-6, atol=0), name
     Np = fa.fa_fp8_vt_stride(N)
     vt = z["vt8"].cpu().numpy()
-    assert vt.shape == (B, H, d, Np) and np.all(vt[..., N:] == 0)
+    assert vt.shape == (B, Hkv, d, Np) and np.all(vt[..., N:] == 0)
     v8 = np.ascontiguousarray(np.swapaxes(vt[..., :N], 2, 3))
     for name, codes, xr, sc in (("q8", z["q8"].cpu().numpy(), oracle.rotate(f64(q), s_np),
                                  z["s_q"].cpu().numpy()[:, :, None, None]),
@@ -49,8 +50,16 @@ def test_quantiser_matches_oracle(N, rot):
                                 ("v8", v8, f64(v), z["s_v"].cpu().numpy()[:, :, None, :])):
         y = xr / sc.astype(np.float64)  # the value in code units, with the GPU's scale
         err = np.abs(oracle.e4m3_decode(codes) - y)
-        # half a gap, plus the fp32 rounding of the GPU's rotation and scaling
-        assert np.all(err <= e4m3_gap(y) / 2 + 1e-5 * np.abs(y) + 1e-6), name
+        # Half a gap, plus the fp32 rounding of the GPU's rotation and scaling. The
+        # rotation is a 128-point Walsh-Hadamard transform in 7 add/subtract stages
+        # after one multiply by sign / sqrt(128) / scale: each step rounds partial
+        # sums whose magnitudes add up to at most sum_j |x_j f_j| <= ||y_row||_2, so
+        # an element is off by at most about 9 u ||y_row||_2 (u = 2^-24) before
+        # its e4m3 rounding, which can then go to the other side of a tie; 2^-20
+        # leaves margin. The 2^-22 |y| term covers the rounding of 1 / scale.
+        row = np.sqrt((y ** 2).sum(axis=-1, keepdims=True))
+        tol = e4m3_gap(y) / 2 + 2.0 ** -20 * row + 2.0 ** -22 * np.abs(y)
+        assert np.all(err <= tol), (name, float((err - tol).max()))
 
 
 def fp8_contract(o, lse, o_ref, lse_ref, o_abs, vsum_abs):
@@ -104,6 +113,70 @@ def test_fp8_forward_within_contract(N, causal, padding):
     fp8_contract(o, lse, o_ref, lse_ref, o_abs, vsum_abs)
 
 
+def dequantised(a):
+    """Q^, K^, V^ (fp64) of codes and scales (q8, k8, v8 [.., N, d], s_q, s_k, s_v)."""
+    qh = oracle.e4m3_decode(a[0]) * a[3][:, :, None, None]
+    kh = oracle.e4m3_decode(a[1]) * a[4][:, :, None, None]
+    vh = oracle.e4m3_decode(a[2]) * a[5][:, :, None, :]
+    return qh, kh, vh
+
+
+@pytest.mark.parametrize("H,Hkv,N,causal,padding", [(8, 2, 1000, True, None),
+                                                    (6, 1, 777, False, (100, 777)),
+                                                    (4, 2, 300, True, (0, 300))])
+def test_fp8_grouped_heads_within_contract(H, Hkv, N, causal, padding):
+    """Grouped K/V heads: q8 [B, H, N, d] with k8, vt8 [B, Hkv, ...]."""
+    B, d = 2, 128
+    xq = inputs.draw_fp8_codes(B, H, N, d, seed=N + H)
+    xk = inputs.draw_fp8_codes(B, Hkv, N, d, seed=N + 100 * Hkv)
+    Np = fa.fa_fp8_vt_stride(N)
+    vt = torch.zeros((B, Hkv, d, Np), dtype=torch.uint8)
+    vt[..., :N] = xk["v8"].transpose(2, 3)
+    sl = None
+    if padding is not None:
+        sl = inputs.draw_small(B, 1, N, 64, seed=N, with_grad=False, padding=padding)["seqlens"]
+    scale = 1.0 / math.sqrt(d)
+    z = dict(q8=xq["q8"].cuda(), k8=xk["k8"].cuda(), vt8=vt.contiguous().cuda(),
+             s_q=xq["s_q"].cuda(), s_k=xk["s_k"].cuda(), s_v=xk["s_v"].cuda())
+    o, lse = fa.fwd_fp8(z, scale, causal=causal, seqlens_k=None if sl is None else sl.cuda())
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    a = [t.numpy() for t in (xq["q8"], xk["k8"], xk["v8"], xq["s_q"].double(),
+                             xk["s_k"].double(), xk["s_v"].double())]
+    sl_np = None if sl is None else sl.numpy()
+    o_ref, lse_ref = oracle.fwd_fp8(*a, scale, causal=causal, seqlens_k=sl_np)
+    qh, kh, vh = dequantised(a)
+    o_abs, _ = oracle.fwd_gqa(qh, kh, np.abs(vh), scale, causal=causal, seqlens_k=sl_np)
+    mean_abs, _ = oracle.fwd_gqa(np.zeros_like(qh), kh, np.abs(vh), scale, causal=causal,
+                                 seqlens_k=sl_np)
+    L = np.full(B, N) if sl_np is None else np.clip(sl_np, 0, N)
+    rows = np.arange(N)
+    count = np.minimum(rows[None, :] + 1, L[:, None]) if causal else np.repeat(L[:, None], N, 1)
+    fp8_contract(o, lse, o_ref, lse_ref, o_abs, mean_abs * count[:, None, :, None])
+
+
+def test_fp8_grouped_heads_equal_repeated_heads():
+    """From bf16 inputs: quantising and running the forward with Hkv K/V heads
+    gives bit for bit what the same calls give with each K/V head repeated for
+    its group (the per-head scales, codes and every product are the same)."""
+    B, H, Hkv, N, d = 2, 6, 2, 700, 128
+    xq = inputs.draw_small(B, H, N, d, seed=41, with_grad=False)
+    xk = inputs.draw_small(B, Hkv, N, d, seed=42, with_grad=False)
+    q, k, v = xq["q"].cuda(), xk["k"].cuda(), xk["v"].cuda()
+    signs = inputs.rotation_signs(d, seed=3).cuda()
+    G = H // Hkv
+    kr, vr = (t.repeat_interleave(G, dim=1).contiguous() for t in (k, v))
+    zg = fa.fp8_quantize(q, k, v, signs)
+    zr = fa.fp8_quantize(q, kr, vr, signs)
+    og, lg = fa.fwd_fp8(zg, 0.09, causal=True)
+    orr, lr = fa.fwd_fp8(zr, 0.09, causal=True)
+    torch.cuda.synchronize()
+    for name in ("k8", "vt8", "s_k", "s_v"):
+        assert torch.equal(zg[name].repeat_interleave(G, dim=1), zr[name]), name
+    assert torch.equal(zg["q8"], zr["q8"]) and torch.equal(zg["s_q"], zr["s_q"])
+    assert torch.equal(og, orr) and torch.equal(lg, lr)
+
+
 def test_fp8_end_to_end_rotation_helps_with_outliers():
     """bf16 inputs whose K has outlier channels: quantised with the rotation the
     FP8 forward lands closer to exact attention than quantised without it, in
@@ -140,3 +213,10 @@ def test_fp8_rejects_bad_arguments():
     assert fa.fa_fwd_fp8(q8, q8, q8, s, s, s, o, lse, 1, 1, 0, 128, 0.125) == \
         fa.FA_ERR_INVALID_ARG
     assert fa.fa_fp8_workspace_size(1, 1, 64) == 0
+    kv = torch.zeros((1, 3, 128, 128), dtype=torch.uint8, device="cuda")
+    q3 = torch.zeros((1, 4, 128, 128), dtype=torch.uint8, device="cuda")
+    o4 = torch.empty((1, 4, 128, 128), dtype=torch.bfloat16, device="cuda")
+    l4 = torch.empty((1, 4, 128), dtype=torch.float32, device="cuda")
+    # 4 query heads cannot share 3 K/V heads
+    assert fa.fa_fwd_fp8_gqa(q3, kv, kv, s, s, s, o4, l4, 1, 4, 3, 128, 128, 0.125) == \
+        fa.FA_ERR_INVALID_ARG
