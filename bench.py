@@ -101,14 +101,14 @@ def load_peaks():
 # Sources each timed kernel is built from: a committed DRAM-traffic figure is
 # used only while these files are unchanged since it was captured.
 KERNEL_SOURCES = {
-    "fwd": ("fa_fwd.cu",),
-    "bwd_dkdv": ("fa_bwd.cu", "fa_bwd_split.cu"),
-    "bwd_dq": ("fa_bwd_split.cu",),
-    "bwd_preprocess": ("fa_bwd.cu",),
-    "decode": ("fa_decode.cu",),
-    "fwd_fp8": ("fa_fwd_fp8.cu",),
+    "fwd": ("fa_fwd.cu", "fa_kernels.h"),
+    "bwd_dkdv": ("fa_bwd.cu", "fa_bwd_split.cu", "fa_kernels.h"),
+    "bwd_dq": ("fa_bwd_split.cu", "fa_kernels.h"),
+    "bwd_preprocess": ("fa_bwd.cu", "fa_kernels.h"),
+    "decode": ("fa_decode.cu", "fa_decode.h"),
+    "fwd_fp8": ("fa_fwd_fp8.cu", "fa_fp8.h"),
 }
-COMMON_SOURCES = ("fa_common.cuh", "sm103_ptx.cuh", "fa_kernels.h")
+COMMON_SOURCES = ("fa_common.cuh", "sm103_ptx.cuh")
 
 
 def kernel_source_hash(kernel=None):

@@ -11,6 +11,8 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_decode.h"
+#include "fa_fp8.h"
 #include "fa_kernels.h"
 
 namespace {

@@ -28,7 +28,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_common.cuh"
-#include "fa_kernels.h"
+#include "fa_decode.h"
 
 namespace fa {
 

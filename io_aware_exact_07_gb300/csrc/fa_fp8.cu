@@ -23,7 +23,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_common.cuh"
-#include "fa_kernels.h"
+#include "fa_fp8.h"
 
 namespace fa {
 
