@@ -13,15 +13,9 @@ import torch
 import oracle
 import io_aware_exact_07_gb300 as fa
 from io_aware_exact_07_gb300 import inputs
-from _parity import LSE_TOL, lse_err
+from _parity import e4m3_code_tol, fp8_contract, fp8_reference_terms
 
 pytestmark = pytest.mark.gpu
-
-def e4m3_gap(y):
-    """Distance between the two e4m3 magnitudes around |y|."""
-    mags = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
-    idx = np.minimum(np.searchsorted(mags, np.abs(y)), len(mags) - 1)
-    return mags[idx] - mags[np.maximum(idx - 1, 0)]
 
 
 @pytest.mark.parametrize("N,rot,Hkv", [(300, True, 3), (1000, True, 3), (129, False, 3),
@@ -50,30 +44,8 @@ def test_quantiser_matches_oracle(N, rot, Hkv):
                                 ("v8", v8, f64(v), z["s_v"].cpu().numpy()[:, :, None, :])):
         y = xr / sc.astype(np.float64)  # the value in code units, with the GPU's scale
         err = np.abs(oracle.e4m3_decode(codes) - y)
-        # Half a gap, plus the fp32 rounding of the GPU's rotation and scaling. The
-        # rotation is a 128-point Walsh-Hadamard transform in 7 add/subtract stages
-        # after one multiply by sign / sqrt(128) / scale: each step rounds partial
-        # sums whose magnitudes add up to at most sum_j |x_j f_j| <= ||y_row||_2, so
-        # an element is off by at most about 9 u ||y_row||_2 (u = 2^-24) before
-        # its e4m3 rounding, which can then go to the other side of a tie; 2^-20
-        # leaves margin. The 2^-22 |y| term covers the rounding of 1 / scale.
-        row = np.sqrt((y ** 2).sum(axis=-1, keepdims=True))
-        tol = e4m3_gap(y) / 2 + 2.0 ** -20 * row + 2.0 ** -22 * np.abs(y)
+        tol = e4m3_code_tol(y)
         assert np.all(err <= tol), (name, float((err - tol).max()))
-
-
-def fp8_contract(o, lse, o_ref, lse_ref, o_abs, vsum_abs):
-    """|O - O^| <= 2^-4 sum P|v^| + 2^-15 sum |v^| + 1.5 bf16 half-ulps; lse 1e-3. The
-    second term: P's e4m3 rounding is absolute (at most 2^-10, half the smallest
-    subnormal) below 2^-6, relative to a row maximum of at least 2^5."""
-    o = o.float().cpu().numpy().astype(np.float64)
-    mag = np.maximum(np.abs(o_ref), 1e-30)
-    half_ulp = np.exp2(np.floor(np.log2(mag)) - 8.0)
-    tol = 2.0 ** -4 * o_abs + 2.0 ** -15 * vsum_abs + 1.5 * half_ulp + 1e-6
-    excess = np.abs(o - o_ref) - tol
-    assert excess.max() <= 0, f"FP8 contract exceeded by {excess.max()}"
-    assert lse_err(lse.cpu().numpy(), lse_ref) <= LSE_TOL
-    return float(np.abs(o - o_ref).max())
 
 
 @pytest.mark.parametrize("N,causal,padding", [(256, False, None), (1000, True, None),
@@ -98,27 +70,7 @@ def test_fp8_forward_within_contract(N, causal, padding):
     a = [t.numpy() for t in (x["q8"], x["k8"], x["v8"], x["s_q"].double(), x["s_k"].double(),
                              x["s_v"].double())]
     sl_np = None if sl is None else sl.numpy()
-    o_ref, lse_ref = oracle.fwd_fp8(*a, scale, causal=causal, seqlens_k=sl_np)
-    vh = oracle.e4m3_decode(a[2]) * a[5][:, :, None, :]
-    qh = oracle.e4m3_decode(a[0]) * a[3][:, :, None, None]
-    kh = oracle.e4m3_decode(a[1]) * a[4][:, :, None, None]
-    o_abs, _ = oracle.fwd(qh, kh, np.abs(vh), scale, causal=causal, seqlens_k=sl_np)
-    # sum over each row's visible keys of |v^|: uniform attention (q = 0) times the count
-    mean_abs, _ = oracle.fwd(np.zeros_like(qh), kh, np.abs(vh), scale, causal=causal,
-                             seqlens_k=sl_np)
-    L = np.full(B, N) if sl_np is None else np.clip(sl_np, 0, N)
-    rows = np.arange(N)
-    count = np.minimum(rows[None, :] + 1, L[:, None]) if causal else np.repeat(L[:, None], N, 1)
-    vsum_abs = mean_abs * count[:, None, :, None]
-    fp8_contract(o, lse, o_ref, lse_ref, o_abs, vsum_abs)
-
-
-def dequantised(a):
-    """Q^, K^, V^ (fp64) of codes and scales (q8, k8, v8 [.., N, d], s_q, s_k, s_v)."""
-    qh = oracle.e4m3_decode(a[0]) * a[3][:, :, None, None]
-    kh = oracle.e4m3_decode(a[1]) * a[4][:, :, None, None]
-    vh = oracle.e4m3_decode(a[2]) * a[5][:, :, None, :]
-    return qh, kh, vh
+    fp8_contract(o, lse, *fp8_reference_terms(a, scale, causal, sl_np))
 
 
 @pytest.mark.parametrize("H,Hkv,N,causal,padding", [(8, 2, 1000, True, None),
@@ -144,15 +96,7 @@ def test_fp8_grouped_heads_within_contract(H, Hkv, N, causal, padding):
     a = [t.numpy() for t in (xq["q8"], xk["k8"], xk["v8"], xq["s_q"].double(),
                              xk["s_k"].double(), xk["s_v"].double())]
     sl_np = None if sl is None else sl.numpy()
-    o_ref, lse_ref = oracle.fwd_fp8(*a, scale, causal=causal, seqlens_k=sl_np)
-    qh, kh, vh = dequantised(a)
-    o_abs, _ = oracle.fwd_gqa(qh, kh, np.abs(vh), scale, causal=causal, seqlens_k=sl_np)
-    mean_abs, _ = oracle.fwd_gqa(np.zeros_like(qh), kh, np.abs(vh), scale, causal=causal,
-                                 seqlens_k=sl_np)
-    L = np.full(B, N) if sl_np is None else np.clip(sl_np, 0, N)
-    rows = np.arange(N)
-    count = np.minimum(rows[None, :] + 1, L[:, None]) if causal else np.repeat(L[:, None], N, 1)
-    fp8_contract(o, lse, o_ref, lse_ref, o_abs, mean_abs * count[:, None, :, None])
+    fp8_contract(o, lse, *fp8_reference_terms(a, scale, causal, sl_np))
 
 
 def test_fp8_grouped_heads_equal_repeated_heads():
