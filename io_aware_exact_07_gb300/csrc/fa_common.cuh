@@ -163,24 +163,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const DropParams& d) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    // one widening multiply gives both halves of each 64-bit product
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+    const uint32_t lo0 = static_cast<uint32_t>(p0), hi0 = static_cast<uint32_t>(p0 >> 32);
+    const uint32_t lo1 = static_cast<uint32_t>(p1), hi1 = static_cast<uint32_t>(p1 >> 32);
     c = make_uint4(hi1 ^ c.y ^ d.rk_lo[r], lo1, hi0 ^ c.w ^ d.rk_hi[r], lo0);
   }
   return c;
-}
-
-// Keep masks for the 16 keys [16*g, 16*g + 16) of query row `row_global`
-// ((b*H + h)*N + i): each byte is 0xFF where the element is kept, 0 where dropped.
-__device__ __forceinline__ uint4 dropout_keep16(const DropParams& d, uint32_t row_global,
-                                                uint32_t key_group) {
-  const uint4 r = philox4x32_10_rk(make_uint4(key_group, row_global, d.off_lo, d.off_hi), d);
-  const uint32_t thr = static_cast<uint32_t>(d.p8) * 0x01010101u;
-  // per-byte unsigned compare: 0xFF where byte >= p8
-  return make_uint4(__vcmpgeu4(r.x, thr), __vcmpgeu4(r.y, thr), __vcmpgeu4(r.z, thr),
-                    __vcmpgeu4(r.w, thr));
 }
 
 // Byte permute: result byte i = byte sel.nibble[i] of the 8-byte value {b, a}
@@ -190,6 +180,25 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
+}
+
+// Keep masks for the 16 keys [16*g, 16*g + 16) of query row `row_global`
+// ((b*H + h)*N + i): each byte is 0xFF where the element is kept, 0 where dropped.
+__device__ __forceinline__ uint4 dropout_keep16(const DropParams& d, uint32_t row_global,
+                                                uint32_t key_group) {
+  const uint4 r = philox4x32_10_rk(make_uint4(key_group, row_global, d.off_lo, d.off_hi), d);
+  const uint32_t thr = static_cast<uint32_t>(d.p8) * 0x01010101u;
+  // Per-byte unsigned compare x >= p8 in SWAR form: the subtraction of the low
+  // seven bits cannot borrow across bytes (bit 7 of each minuend byte is set),
+  // so bit 7 of each byte of dif is [low7(x) >= low7(p8)]; x >= p8 when x's
+  // top bit is set and p8's is not, or when they agree and dif's is set. The
+  // byte permute then spreads each byte's top bit to 0xFF or 0x00.
+  auto ge = [thr](uint32_t x) {
+    const uint32_t dif = (x | 0x80808080u) - (thr & 0x7F7F7F7Fu);
+    const uint32_t top = (x & ~thr) | (~(x ^ thr) & dif);
+    return prmt(top, 0u, 0xBA98u);
+  };
+  return make_uint4(ge(r.x), ge(r.y), ge(r.z), ge(r.w));
 }
 
 // bf16x2 helpers for the epilogues.
