@@ -105,6 +105,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
   using L = FwdLayout<D>;
+  // P in its own buffer (d = 64): without dropout each half of P is stored as
+  // soon as it is formed; with dropout (more live registers) both halves are
+  // stored at the end, which keeps that instance free of spills.
+  constexpr bool kEarlyP = L::kSepP && !DROPOUT;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -630,6 +634,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const uint64_t nm2 = f2_pack(-m_use, -m_use);
           uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums
           uint32_t pk[64];
+          bool pv_ok = true;
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -657,25 +662,44 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 pk[half * 32 + g * 8 + (e >> 1)] = pp;
               }
             }
-            if constexpr (!L::kSepP) tmem_st32(tS + half * 32, &pk[half * 32]);
+            if constexpr (kEarlyP) {
+              // P has its own buffer, which the previous PV reads: once that PV
+              // is done (long before, in steady state), store each half as soon
+              // as it is formed so the store overlaps the next half's exponentials.
+              if (half == 0 && n_done > 0) {
+                if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
+                  pv_ok = false;
+                  break;
+                }
+                ++pv_cnt;
+                tc_fence_after();
+              }
+              tmem_st32(tP + half * 32, &pk[half * 32]);
+            } else if constexpr (!L::kSepP) {
+              tmem_st32(tS + half * 32, &pk[half * 32]);
+            }
+          }
+          if constexpr (L::kSepP && !kEarlyP) {
+            // The previous PV reads the P buffer and accumulates into O: wait for it.
+            if (n_done > 0) {
+              if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
+                pv_ok = false;
+              } else {
+                ++pv_cnt;
+                tc_fence_after();
+              }
+            }
+          }
+          if (!pv_ok) {
+            fail();
+            ok = false;
+            break;
           }
           {
             const uint64_t t2 = f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3]));
             float r0, r1;
             f2_unpack(t2, r0, r1);
             l_sum += r0 + r1;
-          }
-          if constexpr (L::kSepP) {
-            // The previous PV reads the P buffer and accumulates into O: wait for it.
-            if (n_done > 0) {
-              if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
-                fail();
-                ok = false;
-                break;
-              }
-              ++pv_cnt;
-              tc_fence_after();
-            }
           }
           // Rescale the O row in tensor memory (warp-collective loads/stores).
           if (n_done > 0 && __any_sync(0xffffffffu, grow)) {
@@ -689,7 +713,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               tmem_st32(tO + c * 32, o);
             }
           }
-          if constexpr (L::kSepP) {
+          if constexpr (L::kSepP && !kEarlyP) {
             tmem_st32(tP, &pk[0]);
             tmem_st32(tP + 32, &pk[32]);
           }
