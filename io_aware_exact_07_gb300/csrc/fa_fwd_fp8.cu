@@ -493,6 +493,16 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           const uint64_t nm2 = f2_pack(-m_use, -m_use);
           uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
           uint32_t pk[32];  // 128 e4m3 codes, four per word, key order
+          // P row into shared memory, 128-byte swizzle: 16-byte chunk ch at ch ^ (t & 7).
+          // Chunks are stored while the exponentials of the later ones run; the
+          // buffer is free once the previous PV of this tile is done, which is
+          // awaited halfway through the row (that PV has finished by then in
+          // steady state).
+          auto store_chunk = [&](int ch) {
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (t & 7)) << 4)) =
+                make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          };
+          bool pv_ok = true;
 #pragma unroll
           for (int e = 0; e < 128; e += 4) {
             float p0, p1, p2, p3;
@@ -504,6 +514,25 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             p3 = ex2_approx(p3);
             rs2[(e >> 2) & 3] = f2_add(rs2[(e >> 2) & 3], f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
             pk[e >> 2] = e4m3x2(p0, p1) | (e4m3x2(p2, p3) << 16);
+            if (e == 60) {  // first half formed: wait for the buffer, store chunks 0-3
+              if (n_done > 0) {
+                if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
+                  pv_ok = false;
+                  break;
+                }
+                ++pv_cnt;
+                tc_fence_after();
+              }
+#pragma unroll
+              for (int ch = 0; ch < 4; ++ch) store_chunk(ch);
+            } else if (e > 60 && (e & 15) == 12) {
+              store_chunk(e >> 4);
+            }
+          }
+          if (!pv_ok) {
+            fail();
+            ok = false;
+            break;
           }
           {
             const uint64_t t2 = f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3]));
@@ -511,17 +540,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             f2_unpack(t2, r0, r1);
             l_sum += r0 + r1;
           }
-          // the previous PV of this tile has read the P buffer and written O
-          if (n_done > 0) {
-            if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
-              fail();
-              ok = false;
-              break;
-            }
-            ++pv_cnt;
-            tc_fence_after();
-          }
-          if (n_done > 0 && __any_sync(0xffffffffu, grow)) {
+          if (n_done > 0 && __any_sync(0xffffffffu, grow)) {  // the previous PV is done
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               uint32_t o[32];
@@ -533,11 +552,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             }
             tmem_st_wait();
           }
-          // P row into shared memory, 128-byte swizzle: 16-byte chunk ch at ch ^ (t & 7)
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (t & 7)) << 4)) =
-                make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
           fence_async_smem_writes();
           tc_fence_before();
           mbar_arrive(bars.p_full[x]);
