@@ -65,3 +65,29 @@ def test_oracle_philox_matches_curand_host_generator(seed, t0, nblk):
         t = t0 + i
         ctr = [(t >> 16) & 0xFFFFFFFF, t >> 48, t & 0xFFFF, 0]
         assert np.array_equal(oracle.philox4x32_10(ctr, key), blocks[i]), (seed, t)
+
+
+@pytest.mark.parametrize("seed,offset,rows,p", [
+    (0x5EED5EED12345678, 0, [(0, 0), (0, 7), (1, 44)], 0.1),
+    (77, 4321, [(0, 1), (3, 232), (63, 255)], 0.3),   # r = b N + i up to 16383
+])
+def test_oracle_dropout_keep_from_curand_host_blocks(seed, offset, rows, p):
+    """The dropout mapping of include/fa.h (row r = (b H + h) N + i, keys 16 g ..
+    16 g + 15 use the Philox block with counter (g, r, lo32 offset, hi32 offset);
+    key 16 g + e is kept iff byte e of the block, little-endian, is >= p8)
+    rebuilt from cuRAND's host generator: with hi32 offset = 0, r < 2^14 and
+    lo32 offset < 2^16 that block is block t = (r << 48) | (g << 16) | offset of
+    its stream."""
+    lib = _curand()
+    if lib is None:
+        pytest.skip("cuRAND library not found")
+    N = 256
+    p8 = oracle.p8(p)
+    for b, i in rows:
+        keep = oracle.dropout_keep([(b, 0)], 1, N, p, seed=seed, offset=offset)[0, i]
+        r = b * N + i
+        expect = np.zeros(N, dtype=np.uint8)
+        for g in range(N // 16):
+            blk = host_blocks(lib, seed, (r << 48) | (g << 16) | offset, 1)[0]
+            expect[16 * g:16 * g + 16] = (blk.view(np.uint8) >= p8).astype(np.uint8)
+        assert np.array_equal(keep, expect), (b, i)
