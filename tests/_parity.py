@@ -2,7 +2,6 @@
 import math
 
 import numpy as np
-import torch
 
 import oracle
 from io_aware_exact_07_gb300 import inputs

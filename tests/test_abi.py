@@ -93,7 +93,6 @@ def test_host_validation_rejects_bad_arguments(lib):
 
 def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     """Without the built library the binding raises instead of computing elsewhere."""
-    import importlib
     import io_aware_exact_07_gb300 as mod
     monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(mod, "_lib", None)

@@ -4,7 +4,6 @@ sampled heads are checked against the fp64 oracle (O, lse, dQ, dK, dV; for
 grouped K/V heads dK, dV against the oracle's sum over the group), and an
 identity that holds for every head at any size is checked on all of them:
 without dropout each row of P sums to 1, so sum_j dV_j = sum_i dO_i."""
-import numpy as np
 import pytest
 import torch
 

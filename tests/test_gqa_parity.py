@@ -1,7 +1,6 @@
 """Grouped-query attention (shared K/V heads) on the GPU against the fp64 oracle."""
 import math
 
-import numpy as np
 import pytest
 import torch
 

@@ -10,7 +10,6 @@ through an identity that holds at any size without dropout: each row of P
 sums to 1, so the sum over keys of dV equals the sum over query rows of dO."""
 import math
 
-import numpy as np
 import pytest
 import torch
 
