@@ -91,6 +91,23 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.fa_debug_philox(vp(0), a, 4, 0, 0, None) == fa.FA_ERR_INVALID_ARG
 
 
+def test_fp8_grouped_entry_points_validate_on_the_host(lib):
+    # rejected before any device work: H not a multiple of H_kv, H_kv < 1, d != 128
+    vp = ctypes.c_void_p
+    a = vp(1 << 20)
+    quant = lambda H, Hkv, d: lib.fa_fp8_quantize_gqa(a, a, a, None, 1, H, Hkv, 128, d, a, a, a,
+                                                      a, a, a, a, 1 << 20, None)
+    fwd8 = lambda H, Hkv, d: lib.fa_fwd_fp8_gqa(a, a, a, a, a, a, a, a, 1, H, Hkv, 128, d, 0.125,
+                                                0, None, None)
+    for call in (quant, fwd8):
+        assert call(4, 3, 128) == fa.FA_ERR_INVALID_ARG
+        assert call(4, 0, 128) == fa.FA_ERR_INVALID_ARG
+        assert call(4, 2, 64) == fa.FA_ERR_UNSUPPORTED
+    # the H_kv = H entry points are the same calls
+    assert lib.fa_fwd_fp8(a, a, a, a, a, a, a, a, 1, 4, 128, 64, 0.125, 0, None, None) == \
+        fa.FA_ERR_UNSUPPORTED
+
+
 def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     """Without the built library the binding raises instead of computing elsewhere."""
     import io_aware_exact_07_gb300 as mod
