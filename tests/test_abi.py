@@ -108,6 +108,29 @@ def test_fp8_grouped_entry_points_validate_on_the_host(lib):
         fa.FA_ERR_UNSUPPORTED
 
 
+def test_window_and_decode_validate_on_the_host(lib):
+    vp = ctypes.c_void_p
+    a = vp(1 << 20)
+    win = lambda wl, wr: lib.fa_fwd_window(a, a, a, a, a, 1, 1, 1, 128, 64, 0.125, 0, wl, wr, 0.0,
+                                           0, 0, None, None, None)
+    assert win(-2, -1) == fa.FA_ERR_INVALID_ARG
+    assert win(-1, -3) == fa.FA_ERR_INVALID_ARG
+
+    def dec(q=1 << 20, H=8, Hkv=2, Nq=1, d=128, scale=0.125, wl=-1, ctas=4, ws=None, wsb=0):
+        return lib.fa_decode(vp(q), a, a, a, a, 1, H, Hkv, Nq, 1024, d, scale, 0, wl, None, ctas,
+                             ws, wsb, None)
+    # explicit CTA counts: the split is planned without asking the device
+    assert dec(wl=-2) == fa.FA_ERR_INVALID_ARG
+    assert dec(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert dec(q=(1 << 20) + 8) == fa.FA_ERR_INVALID_ARG       # not 16-byte aligned
+    assert dec(Hkv=3) == fa.FA_ERR_INVALID_ARG                 # 8 heads do not share 3
+    assert dec(ctas=-1) == fa.FA_ERR_INVALID_ARG
+    assert dec(Nq=64) == fa.FA_ERR_UNSUPPORTED                 # 4 x 64 rows > one 128-row tile
+    assert dec(d=96) == fa.FA_ERR_UNSUPPORTED
+    # 2 K/V heads x 8 key tiles over 64 CTAs cuts the heads: partial results need a workspace
+    assert dec(ctas=64) == fa.FA_ERR_WORKSPACE
+
+
 def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     """Without the built library the binding raises instead of computing elsewhere."""
     import io_aware_exact_07_gb300 as mod
