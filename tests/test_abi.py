@@ -131,6 +131,16 @@ def test_window_and_decode_validate_on_the_host(lib):
     assert dec(ctas=64) == fa.FA_ERR_WORKSPACE
 
 
+def test_fp8_workspace_covers_grouped_heads(lib):
+    # include/fa.h: fa_fp8_workspace_size(B, H, 128) also covers H_kv < H; the
+    # quantiser uses B*H + 129*B*H_kv 32-bit words (maxima of Q, K and V's columns)
+    for B in (1, 3, 8):
+        for H in range(1, 65):
+            for Hkv in (g for g in range(1, H + 1) if H % g == 0):
+                assert fa.fa_fp8_workspace_size(B, H, 128) >= 4 * (B * H + 129 * B * Hkv)
+    assert fa.fa_fp8_workspace_size(1, 1, 64) == 0
+
+
 def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     """Without the built library the binding raises instead of computing elsewhere."""
     import io_aware_exact_07_gb300 as mod
