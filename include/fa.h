@@ -30,6 +30,9 @@
  *     major, shared by all (b, h): a zero byte at (r, c) removes every pair
  *     with query block r and key block c (FlashAttention deep-read report,
  *     sections 2.6 and 3.5, block-sparse attention; blocks are 128 x 128).
+ *     The C entry points receive only the two pointers and cannot check the
+ *     sizes of these arrays: a shorter seqlens_k or block_mask makes the
+ *     kernels read past its end. (The Python binding checks both shapes.)
  *   - dropout_p in [0, 1): dropout on the normalised probabilities, applied
  *     on chip (deep-read report section 3.2). It is quantised to
  *     p8 = round(256 p) and the effective rate is p8/256 (see fa_dropout_p8).
@@ -297,19 +300,30 @@ fa_status fa_butterfly_mask(uint8_t* mask_host, int nb);
 
 /* Reads the status word of the current device after synchronising `stream`;
  * returns FA_OK or the first device-side error recorded since the last clear.
- * clear != 0 resets it to FA_OK. */
+ * clear != 0 resets it to FA_OK.
+ * The word is one per device, shared by every call on that device: the
+ * forward entry points take no workspace to hold a per-call word. An error
+ * recorded by a kernel on one stream is therefore seen by whichever caller
+ * reads the word next, also from another stream or thread; callers that need
+ * to attribute errors to one call must order their calls and read the word
+ * between them. */
 fa_status fa_device_status(void* stream, int clear);
 
 /* Upper bound on every device-side wait, in nanoseconds (default 4e9). A wait
  * that runs out records FA_ERR_TIMEOUT and the kernel exits early. */
 void fa_set_wait_timeout_ns(uint64_t ns);
 
-/* Test hook for failure detection: mode 1 makes the next forward-type launch
- * (fa_fwd and its _gqa / _window forms, fa_decode, fa_fwd_fp8 and
- * fa_fwd_fp8_gqa) wait on a
- * barrier that nothing completes, so its bounded wait runs out and the kernel
- * returns with FA_ERR_TIMEOUT recorded. The hook is consumed by that launch.
- * mode 0 clears it. */
+/* Test hook for failure detection (host-side injection; nothing faults or
+ * traps on the GPU). The armed launch waits on a barrier that nothing
+ * completes, so its bounded wait runs out and the kernel returns with
+ * FA_ERR_TIMEOUT recorded; the hook is consumed by that launch and later
+ * launches run normally. mode selects the launch:
+ *   1: the next forward-type kernel (fa_fwd and its _gqa / _window forms,
+ *      fa_decode, fa_fwd_fp8, fa_fwd_fp8_gqa);
+ *   2: the next dK/dV kernel (fa_bwd and its _gqa / _window / _noalloc forms,
+ *      fa_bwd_dkdv);
+ *   3: the next dQ kernel (the same backward calls, fa_bwd_dq).
+ * mode 0 (or any other value) clears it. */
 void fa_test_inject_stall(int mode);
 
 /* Static description of an error code. */

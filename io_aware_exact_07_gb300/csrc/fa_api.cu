@@ -162,11 +162,21 @@ fa::DropParams make_drop(float p, uint64_t seed, uint64_t offset) {
   return d;
 }
 
-fa::SyncParams make_sync(const DeviceInfo* di, bool consume_stall) {
+// Launch kinds the stall hook (fa_test_inject_stall) can target.
+enum StallTarget { kStallNone = 0, kStallForward = 1, kStallDkdv = 2, kStallDq = 3 };
+
+// 1 if the stall hook is armed for `target` (and then disarm it), else 0.
+int take_stall(StallTarget target) {
+  if (target == kStallNone) return 0;
+  int expected = static_cast<int>(target);
+  return g_inject_stall.compare_exchange_strong(expected, 0) ? 1 : 0;
+}
+
+fa::SyncParams make_sync(const DeviceInfo* di, StallTarget target) {
   fa::SyncParams s;
   s.status = di->status;
   s.timeout_ns = g_timeout_ns.load();
-  s.inject_stall = consume_stall ? g_inject_stall.exchange(0) : 0;
+  s.inject_stall = take_stall(target);
   return s;
 }
 
@@ -205,7 +215,7 @@ static fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, 
   fa::FwdArgs a;
   a.mask = make_mask(B, H, Hkv, N, causal, block_mask, seqlens_k, wl, wr);
   a.drop = make_drop(dropout_p, seed, offset);
-  a.sync = make_sync(di, true);
+  a.sync = make_sync(di, kStallForward);
   a.scale_log2 = scale * fa::kLog2e;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
@@ -278,7 +288,7 @@ static fa_status bwd_prepare(const void* q, const void* k, const void* v, const 
   }
   a->mask = make_mask(B, H, Hkv, N, causal, block_mask, seqlens_k, wl, wr);
   a->drop = make_drop(dropout_p, seed, offset);
-  a->sync = make_sync(*di, false);
+  a->sync = make_sync(*di, kStallNone);
   a->scale = scale;
   a->scale_log2 = scale * fa::kLog2e;
   a->o = static_cast<const __nv_bfloat16*>(o);
@@ -307,8 +317,14 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool drop = a.drop.p8 > 0;
   cudaError_t e = fa::launch_bwd_preprocess(a, d, di->num_sms, s);
-  if (e == cudaSuccess) e = fa::launch_bwd_dkdv(m[0], m[1], m[2], m[3], a, d, drop, di->num_sms, s);
-  if (e == cudaSuccess) e = fa::launch_bwd_dq(m[0], m[1], m[2], m[3], a, d, drop, di->num_sms, s);
+  if (e == cudaSuccess) {
+    a.sync.inject_stall = take_stall(kStallDkdv);
+    e = fa::launch_bwd_dkdv(m[0], m[1], m[2], m[3], a, d, drop, di->num_sms, s);
+  }
+  if (e == cudaSuccess) {
+    a.sync.inject_stall = take_stall(kStallDq);
+    e = fa::launch_bwd_dq(m[0], m[1], m[2], m[3], a, d, drop, di->num_sms, s);
+  }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -370,6 +386,7 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
                              causal, -1, -1, dropout_p, seed, offset, block_mask, seqlens_k,
                              workspace, workspace_bytes, 2, &a, m, &di);
   if (st != FA_OK) return st;
+  a.sync.inject_stall = take_stall(kStallDkdv);
   return fa::launch_bwd_dkdv(m[0], m[1], m[2], m[3], a, d, a.drop.p8 > 0, di->num_sms,
                              static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FA_OK
@@ -388,6 +405,7 @@ fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dou
                              scale, causal, -1, -1, dropout_p, seed, offset, block_mask,
                              seqlens_k, workspace, workspace_bytes, 4, &a, m, &di);
   if (st != FA_OK) return st;
+  a.sync.inject_stall = take_stall(kStallDq);
   return fa::launch_bwd_dq(m[0], m[1], m[2], m[3], a, d, a.drop.p8 > 0, di->num_sms,
                            static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FA_OK
@@ -517,7 +535,7 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
   a.per_cta = p.per_cta;
   a.seg_max = p.seg_max;
   a.scale_log2 = scale * fa::kLog2e;
-  a.sync = make_sync(di, true);
+  a.sync = make_sync(di, kStallForward);
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   const size_t slots = static_cast<size_t>(B) * H * Nq * p.seg_max;
@@ -601,7 +619,7 @@ fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* vt8, const 
     return FA_ERR_CUDA;
   fa::Fp8FwdArgs a;
   a.mask = make_mask(B, H, Hkv, N, causal, nullptr, seqlens_k);
-  a.sync = make_sync(di, true);
+  a.sync = make_sync(di, kStallForward);
   a.scale_log2 = scale * fa::kLog2e;
   a.s_q = s_q;
   a.s_k = s_k;
@@ -688,7 +706,9 @@ fa_status fa_device_status(void* stream, int clear) {
 
 void fa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 
-void fa_test_inject_stall(int mode) { g_inject_stall.store(mode ? 1 : 0); }
+void fa_test_inject_stall(int mode) {
+  g_inject_stall.store(mode >= kStallForward && mode <= kStallDq ? mode : kStallNone);
+}
 
 const char* fa_status_string(fa_status s) {
   switch (s) {

@@ -95,7 +95,7 @@ struct DkdvLayout {
   static constexpr int kDsumOff = kLseOff + kStages * 512;          // kStages x 128 fp32
   static constexpr int kDropOff = kDsumOff + kStages * 512;         // 8 warps x 2 KB Philox scratch
   static constexpr int kBarOff = kDropOff + 8 * 2048;
-  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 1;
+  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
   __device__ static constexpr uint32_t col_dv() { return 0u; }
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* dsum_s = reinterpret_cast<float*>(smem + L::kDsumOff);
 
   uint32_t b_kv_full, b_kv_empty, b_q_full[4], b_q_empty[4], b_st_full, b_dpt_full, b_p_ready,
-      b_ds_ready, b_acc_full, b_acc_free, b_drain;
+      b_ds_ready, b_acc_full, b_acc_free, b_drain, b_stall;
   {
     int i = 0;
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     b_acc_full = nb();
     b_acc_free = nb();
     b_drain = nb();
+    b_stall = nb();  // test hook: never completed
   }
   if (tid == 0) {
     *abort_flag = 0;
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(b_acc_full, 1);
     mbar_init(b_acc_free, 256);
     mbar_init(b_drain, 1);
+    mbar_init(b_stall, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -262,6 +264,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool elected = lane == 0;
     uint32_t it = 0, p_cnt = 0, ds_cnt = 0;
     bool ok = true;
+    if (args.sync.inject_stall && elected) {
+      // Test hook: this barrier is never completed, so the bounded wait runs out.
+      if (!mbar_wait(b_stall, 0, tmo, abort_flag)) {
+        fail();
+        ok = false;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
     int unit_count = 0;
     // acc (+)= A[tmem, 64-column halves at a0 and a0 + 64] * B[smem, MN-major]
     auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base, bool accumulate) {

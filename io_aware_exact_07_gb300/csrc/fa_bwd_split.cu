@@ -99,7 +99,7 @@ struct DkdvL {
   static constexpr int kDsumOff = kLseOff + kStages * 512;
   static constexpr int kDropOff = kDsumOff + kStages * 512;          // 16 warps x 1 KB
   static constexpr int kBarOff = kDropOff + kComputeWarps * 1024;
-  static constexpr int kNumBars = 4 + 2 * kMaxQStages + 12;
+  static constexpr int kNumBars = 4 + 2 * kMaxQStages + 13;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColSt = 2 * D, kColDPt = 2 * D + 128;
@@ -112,6 +112,7 @@ struct DkdvBars {
   uint32_t kv_full[2], kv_empty[2], q_full[kMaxQStages], q_empty[kMaxQStages];
   uint32_t st_full, st_free, dpt_full, dpt_free, p_ready, p_done, ds_ready, ds_done;
   uint32_t acc_full, acc_free, drain_a, drain_b;
+  uint32_t stall;  // test hook: never completed
 };
 
 template <int D, bool DROPOUT, bool GQA, bool WIN>
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.acc_free = nb();
     bars.drain_a = nb();
     bars.drain_b = nb();
+    bars.stall = nb();
   }
   if (tid == 0) {
     *abort_flag = 0;
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bars.acc_free, kComputeThreads);
     mbar_init(bars.drain_a, 1);
     mbar_init(bars.drain_b, 1);
+    mbar_init(bars.stall, 1);
     fence_mbar_init();
   }
   if (warp == kIssueAWarp) {
@@ -281,6 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_dp_ok = L::kSepBuf ? bars.dpt_free : bars.ds_done;
     uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
     bool ok = true;
+    if (args.sync.inject_stall && leader) {
+      // Test hook: this barrier is never completed, so the bounded wait runs out.
+      if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
+        fail();
+        ok = false;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
@@ -648,7 +659,7 @@ struct DqL {
   static constexpr int kKOff = kQDBufs * 2 * T;
   static constexpr int kVOff = kKOff + kKStages * T;
   static constexpr int kBarOff = kVOff + kVStages * T;
-  static constexpr int kNumBars = 4 + 2 * kMaxKStages + 2 * kMaxVStages + 10;
+  static constexpr int kNumBars = 4 + 2 * kMaxKStages + 2 * kMaxVStages + 11;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
@@ -659,6 +670,7 @@ struct DqBars {
   uint32_t v_full[kMaxVStages], v_empty[kMaxVStages];
   uint32_t s_full, s_free, dp_full, dp_free, ds_ready, ds_done, dq_full, dq_free;
   uint32_t drain_a, drain_b;
+  uint32_t stall;  // test hook: never completed
 };
 
 template <int D, bool DROPOUT, bool WIN>
@@ -704,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.dq_free = nb();
     bars.drain_a = nb();
     bars.drain_b = nb();
+    bars.stall = nb();
   }
   if (tid == 0) {
     *abort_flag = 0;
@@ -729,6 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bars.dq_free, kComputeThreads);
     mbar_init(bars.drain_a, 1);
     mbar_init(bars.drain_b, 1);
+    mbar_init(bars.stall, 1);
     fence_mbar_init();
   }
   if (warp == kIssueAWarp) {
@@ -828,6 +842,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = lane == 0;
     uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
     bool ok = true;
+    if (args.sync.inject_stall && leader) {
+      // Test hook: this barrier is never completed, so the bounded wait runs out.
+      if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
+        fail();
+        ok = false;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
       int bh, qt;
