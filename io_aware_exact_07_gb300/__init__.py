@@ -176,12 +176,19 @@ def _kv_heads(q, k, v) -> int:
     return Hkv
 
 
-def _opt_ptrs(block_mask, seqlens_k):
-    if block_mask is not None and (block_mask.dtype != torch.uint8 or not block_mask.is_cuda
-                                   or not block_mask.is_contiguous()):
-        raise ValueError("block_mask must be a contiguous uint8 CUDA tensor [nb, nb]")
-    if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda):
-        raise ValueError("seqlens_k must be an int32 CUDA tensor [B]")
+def _opt_ptrs(block_mask, seqlens_k, B, N):
+    """Pointers of the optional block mask (uint8 [nb, nb], nb = ceil(N / 128))
+    and key lengths (int32 [B]). The kernels index both without bounds (the C
+    entry points cannot know their sizes), so their shapes are checked here."""
+    if block_mask is not None:
+        nb = (int(N) + 127) // 128
+        if (block_mask.dtype != torch.uint8 or not block_mask.is_cuda
+                or not block_mask.is_contiguous() or tuple(block_mask.shape) != (nb, nb)):
+            raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor [{nb}, {nb}]")
+    if seqlens_k is not None:
+        if (seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda
+                or not seqlens_k.is_contiguous() or tuple(seqlens_k.shape) != (int(B),)):
+            raise ValueError(f"seqlens_k must be a contiguous int32 CUDA tensor [{int(B)}]")
     return _ptr(block_mask), _ptr(seqlens_k)
 
 
@@ -189,7 +196,7 @@ def _opt_ptrs(block_mask, seqlens_k):
 
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal=False, dropout_p=0.0, seed=0, offset=0,
            block_mask=None, seqlens_k=None, stream=None) -> int:
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
                          int(bool(causal)), float(dropout_p), int(seed), int(offset), bm, sl,
                          _stream(stream))
@@ -202,7 +209,7 @@ def fa_bwd_workspace_size(B, H, N, d) -> int:
 def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal=False, dropout_p=0.0,
            seed=0, offset=0, block_mask=None, seqlens_k=None, workspace=None, workspace_bytes=0,
            stream=None) -> int:
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
                          _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                          float(dropout_p), int(seed), int(offset), bm, sl, _ptr(workspace),
@@ -211,7 +218,7 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal=False, d
 
 def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal=False, dropout_p=0.0, seed=0,
                offset=0, block_mask=None, seqlens_k=None, stream=None) -> int:
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N, d,
                              float(scale), int(bool(causal)), float(dropout_p), int(seed),
                              int(offset), bm, sl, _stream(stream))
@@ -220,7 +227,7 @@ def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal=False, dropout_p
 def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal=False,
                dropout_p=0.0, seed=0, offset=0, block_mask=None, seqlens_k=None, workspace=None,
                workspace_bytes=0, stream=None) -> int:
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
                              _ptr(dk), _ptr(dv), B, H, H_kv, N, d, float(scale),
                              int(bool(causal)), float(dropout_p), int(seed), int(offset), bm, sl,
@@ -230,7 +237,7 @@ def fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causa
 def fa_fwd_window(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal=False, window_left=-1,
                   window_right=-1, dropout_p=0.0, seed=0, offset=0, block_mask=None,
                   seqlens_k=None, stream=None) -> int:
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N, d,
                                 float(scale), int(bool(causal)), int(window_left),
                                 int(window_right), float(dropout_p), int(seed), int(offset), bm,
@@ -241,7 +248,7 @@ def fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, d, scale, ca
                   window_left=-1, window_right=-1, dropout_p=0.0, seed=0, offset=0,
                   block_mask=None, seqlens_k=None, workspace=None, workspace_bytes=0,
                   stream=None) -> int:
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, H_kv, N, d, float(scale),
                                 int(bool(causal)), int(window_left), int(window_right),
@@ -257,7 +264,7 @@ def fa_bwd_preprocess(o, dout, B, H, N, d, workspace, workspace_bytes, stream=No
 def fa_bwd_dkdv(q, k, v, dout, lse, dk, dv, B, H, N, d, scale, causal=False, dropout_p=0.0,
                 seed=0, offset=0, block_mask=None, seqlens_k=None, workspace=None,
                 workspace_bytes=0, stream=None) -> int:
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(dk),
                               _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                               float(dropout_p), int(seed), int(offset), bm, sl, _ptr(workspace),
@@ -267,7 +274,7 @@ def fa_bwd_dkdv(q, k, v, dout, lse, dk, dv, B, H, N, d, scale, causal=False, dro
 def fa_bwd_dq(q, k, v, dout, lse, dq, B, H, N, d, scale, causal=False, dropout_p=0.0, seed=0,
               offset=0, block_mask=None, seqlens_k=None, workspace=None, workspace_bytes=0,
               stream=None) -> int:
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(dq), B, H, N,
                             d, float(scale), int(bool(causal)), float(dropout_p), int(seed),
                             int(offset), bm, sl, _ptr(workspace), int(workspace_bytes),
@@ -279,7 +286,7 @@ def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal=
                    stream=None) -> int:
     """fa_bwd for callers that cannot allocate device memory: the library uses
     its own static device scratch (B*H*N <= 2^22) instead of a workspace."""
-    bm, sl = _opt_ptrs(block_mask, seqlens_k)
+    bm, sl = _opt_ptrs(block_mask, seqlens_k, B, N)
     return load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                                  _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
                                  int(bool(causal)), float(dropout_p), int(seed), int(offset), bm,
@@ -294,8 +301,9 @@ def fa_decode(q, k_cache, v_cache, o, lse, B, H, H_kv, Nq, Nk, d, scale, causal=
               seqlens_k=None, num_ctas=0, workspace=None, workspace_bytes=0, stream=None,
               window_left=-1) -> int:
     if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda
-                                  or not seqlens_k.is_contiguous()):
-        raise ValueError("seqlens_k must be a contiguous int32 CUDA tensor")
+                                  or not seqlens_k.is_contiguous()
+                                  or tuple(seqlens_k.shape) != (int(B),)):
+        raise ValueError(f"seqlens_k must be a contiguous int32 CUDA tensor [{int(B)}]")
     return load().fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, H, H_kv,
                             Nq, Nk, d, float(scale), int(bool(causal)), int(window_left),
                             _ptr(seqlens_k), int(num_ctas), _ptr(workspace), int(workspace_bytes),
@@ -319,7 +327,7 @@ def fa_fp8_quantize(q, k, v, signs, B, H, N, d, q8, k8, vt8, s_q, s_k, s_v, work
 
 def fa_fwd_fp8(q8, k8, vt8, s_q, s_k, s_v, o, lse, B, H, N, d, scale, causal=False,
                seqlens_k=None, stream=None) -> int:
-    _, sl = _opt_ptrs(None, seqlens_k)
+    _, sl = _opt_ptrs(None, seqlens_k, B, N)
     return load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(s_q), _ptr(s_k), _ptr(s_v),
                              _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)), sl,
                              _stream(stream))
@@ -335,7 +343,7 @@ def fa_fp8_quantize_gqa(q, k, v, signs, B, H, Hkv, N, d, q8, k8, vt8, s_q, s_k, 
 
 def fa_fwd_fp8_gqa(q8, k8, vt8, s_q, s_k, s_v, o, lse, B, H, Hkv, N, d, scale, causal=False,
                    seqlens_k=None, stream=None) -> int:
-    _, sl = _opt_ptrs(None, seqlens_k)
+    _, sl = _opt_ptrs(None, seqlens_k, B, N)
     return load().fa_fwd_fp8_gqa(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(s_q), _ptr(s_k), _ptr(s_v),
                                  _ptr(o), _ptr(lse), B, H, Hkv, N, d, float(scale),
                                  int(bool(causal)), sl, _stream(stream))

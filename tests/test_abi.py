@@ -170,3 +170,28 @@ def test_decode_workspace_size(lib):
     assert fa.fa_decode_workspace_size(1, 4, 2, 1, 300, 96, 4) == 0       # d
     assert fa.fa_decode_workspace_size(1, 4, 2, 1, 0, 64, 4) == 0         # empty cache dim
 
+
+
+@pytest.mark.gpu
+def test_binding_checks_the_shapes_of_block_mask_and_key_lengths(lib):
+    """The kernels index block_mask [nb, nb] and seqlens_k [B] without bounds,
+    so the binding refuses wrongly sized ones before any launch."""
+    import torch
+    B, H, N, d = 2, 1, 300, 64  # nb = 3
+    q = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    good_bm = torch.ones((3, 3), dtype=torch.uint8, device="cuda")
+    good_sl = torch.full((B,), N, dtype=torch.int32, device="cuda")
+    fa.fwd(q, q, q, block_mask=good_bm, seqlens_k=good_sl)
+    for bm in (torch.ones((2, 2), dtype=torch.uint8, device="cuda"),
+               torch.ones((9,), dtype=torch.uint8, device="cuda"),
+               torch.ones((3, 6), dtype=torch.uint8, device="cuda")[:, ::2]):
+        with pytest.raises(ValueError):
+            fa.fwd(q, q, q, block_mask=bm)
+    for sl in (torch.full((1,), N, dtype=torch.int32, device="cuda"),
+               torch.full((B, 1), N, dtype=torch.int32, device="cuda"),
+               torch.full((B,), N, dtype=torch.int64, device="cuda")):
+        with pytest.raises(ValueError):
+            fa.fwd(q, q, q, seqlens_k=sl)
+        with pytest.raises(ValueError):
+            fa.decode(q[:, :, :1], q, q, seqlens_k=sl)
+    torch.cuda.synchronize()
