@@ -129,3 +129,25 @@ def fp8_reference_terms(a, scale, causal, seqlens_k=None):
     rows = np.arange(N)
     count = np.minimum(rows[None, :] + 1, L[:, None]) if causal else np.repeat(L[:, None], N, 1)
     return o_ref, lse_ref, o_abs, mean_abs * count[:, None, :, None]
+
+
+def check_grads_per_head(named):
+    """named: (name, gpu, oracle) triples of [..., N, d] gradients. The relative
+    Frobenius error is taken head by head over the leading axes, so one bad
+    head cannot hide under the norm of the others. A head whose exact
+    gradient is zero (one visible key: dS = P (dP - D) = 0; a key no query
+    sees) must come back within 1e-2 of zero: its GPU value is the bf16
+    rounding residue of D = rowsum(dO * O)."""
+    for name, g, r in named:
+        g = np.asarray(g, dtype=np.float64)
+        r = np.asarray(r, dtype=np.float64)
+        assert g.shape == r.shape, name
+        assert np.isfinite(g).all(), name
+        gh = g.reshape(-1, *g.shape[-2:])
+        rh = r.reshape(-1, *r.shape[-2:])
+        for n in range(gh.shape[0]):
+            if np.linalg.norm(rh[n]) == 0:
+                assert np.abs(gh[n]).max() <= 1e-2, f"{name} head {n}"
+                continue
+            e = rel_fro(gh[n], rh[n])
+            assert e <= GRAD_RTOL, f"{name} head {n}: relative Frobenius error {e}"
