@@ -40,7 +40,9 @@ from io_aware_exact_07_gb300 import inputs  # noqa: E402
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
 UNIT = "TFLOP/s"
-DEFAULT_WORKLOAD = "gpt2_medium"
+# The largest single-GPU workload of the suite, and one of those the forward /
+# backward tensor-core targets (N >= 4K) apply to; the others run with --workload.
+DEFAULT_WORKLOAD = "long_16k_d128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 # algorithmic flops per allowed pair for each tensor-core kernel (per unit of d)
@@ -469,16 +471,18 @@ def run_ours(args, w):
     total_k = sum(kstats.values())
     dominant = max(kstats, key=lambda k: kstats[k])
     if dominant in KERNEL_FLOPS_PER_PAIR_D:
+        # the kernel runs a few milliseconds at a time: its denominator is the
+        # burst peak; the fraction of the sustained (power-capped) one is kept beside it
         ach = KERNEL_FLOPS_PER_PAIR_D[dominant] * w.d * pairs / kstats[dominant] / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": ach / peak_sus}
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": ach / peak_burst, "frac_of_sustained": ach / peak_sus}
     else:
         rows = w.B * w.H * w.N
         byts = 2 * rows * w.d * 2 + rows * 4
         ach = byts / kstats[dominant] / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
     roof["kernel"] = dominant
-    roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
+    roof["peak_source"] = f"{peak_src} ({'bf16_tflops' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
     roof["traffic"] = ncu_traffic(dominant, w.name)
     value = whole_job_value(flops_step, args.steps, world, elapsed)
     fwd_t, bwd_t = kstats["fwd"], total_k - kstats["fwd"]
