@@ -96,6 +96,8 @@ def _block_mask(N, seed):
     nb = math.ceil(N / 128)
     g = np.random.default_rng(seed)
     m = (g.random((nb, nb)) < 0.6).astype(np.uint8)
+    for r in range(1, nb):
+        m[r, r] = 1   # every diagonal block but the first: causal cases keep some pairs
     m[nb - 1, :] = 0  # a query block that sees no key
     m[:, 0] = 0       # a key block that no query sees
     m[0, 1 % nb] = 1
