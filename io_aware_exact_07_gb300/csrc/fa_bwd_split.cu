@@ -32,7 +32,18 @@ constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kProdWarp = 16;
 constexpr int kIssueAWarp = 17;
 constexpr int kIssueBWarp = 18;
-constexpr int kThreads = 19 * 32;
+// Warp 19 idles: it completes the fifth warpgroup, since registers move between
+// whole warpgroups.
+constexpr int kThreads = 20 * 32;
+// Registers per thread: 96 at launch (five warps per sub-partition); the producer
+// and issuer warpgroup gives most of its share to the compute warps, which keep
+// the per-step P^T / dS^T values of 32 columns live.
+constexpr int kRegsLaunch = 96;
+constexpr int kRegsCompute = 104;
+constexpr int kRegsAux = 56;
+static_assert(kComputeThreads * kRegsCompute + (kThreads - kComputeThreads) * kRegsAux <=
+                  kThreads * kRegsLaunch,
+              "register reallocation exceeds the block's launch allocation");
 
 template <int D>
 struct TileT {
@@ -205,208 +216,214 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::kQOff);
   const uint32_t sDO = smem_u32(smem + L::kDOOff);
 
-  if (warp == kProdWarp) {
-    // ------------------------------------------------------------ producer
-    uint32_t it = 0, q_arms = 0, kv_arms[2] = {0, 0};
-    bool ok = true;
-    int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
-      const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      const int kb = unit_count % L::kKVBufs;
-      const int kuse = unit_count / L::kKVBufs;
-      if (kuse > 0 && !mbar_wait_warp(bars.kv_empty[kb], (kuse - 1) & 1, tmo, abort_flag)) {
-        fail();
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        mbar_expect_tx(bars.kv_full[kb], 2 * T);
-        tma_tile<D>(sKV + (2 * kb) * T, &tm_k, kt * kTile, bhk, bars.kv_full[kb]);
-        tma_tile<D>(sKV + (2 * kb + 1) * T, &tm_v, kt * kTile, bhk, bars.kv_full[kb]);
-      }
-      ++kv_arms[kb];
-      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
-             ++bh) {  // the query heads sharing this K/V head
-        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
-          while (bits != 0u) {
-            const int qt = chunk * 32 + (__ffs(bits) - 1);
-            bits &= bits - 1;
-            const int s = it % L::kStages;
-            const uint32_t ph = (it / L::kStages) & 1u;
-            if (!mbar_wait_warp(bars.q_empty[s], ph ^ 1u, tmo, abort_flag)) {
-              fail();
-              ok = false;
-              break;
-            }
-            float4 l4, d4;
-            float* lp = &l4.x;
-            float* dp = &d4.x;
-  #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int row = qt * kTile + 4 * lane + r;
-              const bool in = row < N;
-              const long long idx = static_cast<long long>(bh) * N + row;
-              lp[r] = -lse2_at(args.lse, idx, in);
-              dp[r] = in ? -args.dsum[idx] : 0.f;
-            }
-            // staged negated: the compute warps add them as packed pairs
-            reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
-            reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
-            if (lane == 0) {
-              mbar_expect_tx(bars.q_full[s], 2 * T);
-              tma_tile<D>(sQ + s * T, &tm_q, qt * kTile, bh, bars.q_full[s]);
-              tma_tile<D>(sDO + s * T, &tm_do, qt * kTile, bh, bars.q_full[s]);
-            } else {
-              mbar_arrive(bars.q_full[s]);
-            }
-            ++q_arms;
-            ++it;
-          }
+  if (warp >= kComputeWarps) {
+    // producer, issuers and the idle warp: one warpgroup, which hands most of its
+    // registers to the compute warpgroups
+    regs_dec<kRegsAux>();
+    if (warp == kProdWarp) {
+      // ------------------------------------------------------------ producer
+      uint32_t it = 0, q_arms = 0, kv_arms[2] = {0, 0};
+      bool ok = true;
+      int unit_count = 0;
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+        const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+        const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        const int kb = unit_count % L::kKVBufs;
+        const int kuse = unit_count / L::kKVBufs;
+        if (kuse > 0 && !mbar_wait_warp(bars.kv_empty[kb], (kuse - 1) & 1, tmo, abort_flag)) {
+          fail();
+          ok = false;
+          break;
         }
-      }
-    }
-    for (int b = 0; b < L::kKVBufs; ++b)
-      if (kv_arms[b]) mbar_wait_warp(bars.kv_full[b], (kv_arms[b] - 1) & 1, tmo, nullptr);
-#pragma unroll
-    for (int s = 0; s < L::kStages; ++s)
-      if (q_arms > static_cast<uint32_t>(s))
-        mbar_wait_warp(bars.q_full[s], ((q_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
-  } else if (warp == kIssueAWarp) {
-    // ------------------------------------------------------------ S^T, dP^T issuer
-    // Before overwriting S^T (dP^T) it waits until the compute warps have read it
-    // (separate buffers), or until dV (dK) has consumed the P^T (dS^T) written
-    // over it (aliased buffers).
-    const bool leader = lane == 0;
-    const uint32_t bar_s_ok = L::kSepBuf ? bars.st_free : bars.p_done;
-    const uint32_t bar_dp_ok = L::kSepBuf ? bars.dpt_free : bars.ds_done;
-    uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
-    bool ok = true;
-    if (args.sync.inject_stall && leader) {
-      // Test hook: this barrier is never completed, so the bounded wait runs out.
-      if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
-        fail();
-        ok = false;
-      }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
-      const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      const int kb = unit_count % L::kKVBufs;
-      if (leader &&
-          !mbar_wait(bars.kv_full[kb], (unit_count / L::kKVBufs) & 1, tmo, abort_flag)) {
-        fail();
-        ok = false;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      const uint64_t dK = sdesc_sw128(sKV + (2 * kb) * T, 16, 1024);
-      const uint64_t dV = sdesc_sw128(sKV + (2 * kb + 1) * T, 16, 1024);
-      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
-             ++bh) {  // the query heads sharing this K/V head
-        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          const uint32_t vbits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
-          if (leader) {
-            for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
+        if (lane == 0) {
+          mbar_expect_tx(bars.kv_full[kb], 2 * T);
+          tma_tile<D>(sKV + (2 * kb) * T, &tm_k, kt * kTile, bhk, bars.kv_full[kb]);
+          tma_tile<D>(sKV + (2 * kb + 1) * T, &tm_v, kt * kTile, bhk, bars.kv_full[kb]);
+        }
+        ++kv_arms[kb];
+        for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+               ++bh) {  // the query heads sharing this K/V head
+          for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+            uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
+            while (bits != 0u) {
+              const int qt = chunk * 32 + (__ffs(bits) - 1);
+              bits &= bits - 1;
               const int s = it % L::kStages;
               const uint32_t ph = (it / L::kStages) & 1u;
-              if (!mbar_wait(bars.q_full[s], ph, tmo, abort_flag) ||
-                  (gt > 0 && !mbar_wait(bar_s_ok, sfc++ & 1, tmo, abort_flag))) {
+              if (!mbar_wait_warp(bars.q_empty[s], ph ^ 1u, tmo, abort_flag)) {
+                fail();
                 ok = false;
                 break;
               }
-              tc_fence_after();
-              mma_ss_tile<D>(tmem + L::kColSt, dK, sdesc_sw128(sQ + s * T, 16, 1024));
-              mma_commit(bars.st_full);
-              if (gt > 0 && !mbar_wait(bar_dp_ok, dfc++ & 1, tmo, abort_flag)) {
-                ok = false;
-                break;
+              float4 l4, d4;
+              float* lp = &l4.x;
+              float* dp = &d4.x;
+    #pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const int row = qt * kTile + 4 * lane + r;
+                const bool in = row < N;
+                const long long idx = static_cast<long long>(bh) * N + row;
+                lp[r] = -lse2_at(args.lse, idx, in);
+                dp[r] = in ? -args.dsum[idx] : 0.f;
               }
-              tc_fence_after();
-              mma_ss_tile<D>(tmem + L::kColDPt, dV, sdesc_sw128(sDO + s * T, 16, 1024));
-              mma_commit(bars.dpt_full);
-              mma_commit(bars.q_empty[s]);
-              ++gt;
+              // staged negated: the compute warps add them as packed pairs
+              reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
+              reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
+              if (lane == 0) {
+                mbar_expect_tx(bars.q_full[s], 2 * T);
+                tma_tile<D>(sQ + s * T, &tm_q, qt * kTile, bh, bars.q_full[s]);
+                tma_tile<D>(sDO + s * T, &tm_do, qt * kTile, bh, bars.q_full[s]);
+              } else {
+                mbar_arrive(bars.q_full[s]);
+              }
+              ++q_arms;
               ++it;
             }
-            if (!ok) fail();
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
         }
       }
-      if (leader && ok) mma_commit(bars.kv_empty[kb]);
-    }
-    if (leader) {
-      mma_commit(bars.drain_a);
-      mbar_wait(bars.drain_a, 0, tmo, nullptr);
-    }
-    __syncwarp();
-  } else if (warp == kIssueBWarp) {
-    // ------------------------------------------------------------ dV, dK issuer
-    const bool leader = lane == 0;
-    uint32_t it = 0, prc = 0, dsc = 0;
-    bool ok = true;
-    int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
-      const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      bool first = true;
-      for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
-             ++bh) {  // the query heads sharing this K/V head
-        for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
-          const uint32_t vbits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
-          if (leader) {
-            for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
-              const int s = it % L::kStages;
-              if (!mbar_wait(bars.p_ready, prc++ & 1, tmo, abort_flag) ||
-                  (first && unit_count > 0 &&
-                   !mbar_wait(bars.acc_free, (unit_count - 1) & 1, tmo, abort_flag))) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              mma_ts_tile<D>(tmem + L::kColDV, tmem + L::kColP, L::kPair,
-                             sdesc_sw128(sDO + s * T, 16384, 1024), !first);
-              mma_commit(bars.p_done);
-              if (!mbar_wait(bars.ds_ready, dsc++ & 1, tmo, abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              mma_ts_tile<D>(tmem + L::kColDK, tmem + L::kColDS, L::kPair,
-                             sdesc_sw128(sQ + s * T, 16384, 1024), !first);
-              mma_commit(bars.ds_done);
-              mma_commit(bars.q_empty[s]);
-              first = false;
-              ++it;
-            }
-            if (!ok) fail();
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
-      }
-      if (leader && ok) {
-        if (first && unit_count > 0 &&
-            !mbar_wait(bars.acc_free, (unit_count - 1) & 1, tmo, abort_flag)) {
-          ok = false;
+      for (int b = 0; b < L::kKVBufs; ++b)
+        if (kv_arms[b]) mbar_wait_warp(bars.kv_full[b], (kv_arms[b] - 1) & 1, tmo, nullptr);
+  #pragma unroll
+      for (int s = 0; s < L::kStages; ++s)
+        if (q_arms > static_cast<uint32_t>(s))
+          mbar_wait_warp(bars.q_full[s], ((q_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
+    } else if (warp == kIssueAWarp) {
+      // ------------------------------------------------------------ S^T, dP^T issuer
+      // Before overwriting S^T (dP^T) it waits until the compute warps have read it
+      // (separate buffers), or until dV (dK) has consumed the P^T (dS^T) written
+      // over it (aliased buffers).
+      const bool leader = lane == 0;
+      const uint32_t bar_s_ok = L::kSepBuf ? bars.st_free : bars.p_done;
+      const uint32_t bar_dp_ok = L::kSepBuf ? bars.dpt_free : bars.ds_done;
+      uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
+      bool ok = true;
+      if (args.sync.inject_stall && leader) {
+        // Test hook: this barrier is never completed, so the bounded wait runs out.
+        if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
           fail();
-        } else {
-          mma_commit(bars.acc_full);
+          ok = false;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      int unit_count = 0;
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+        const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+        const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        const int kb = unit_count % L::kKVBufs;
+        if (leader &&
+            !mbar_wait(bars.kv_full[kb], (unit_count / L::kKVBufs) & 1, tmo, abort_flag)) {
+          fail();
+          ok = false;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        const uint64_t dK = sdesc_sw128(sKV + (2 * kb) * T, 16, 1024);
+        const uint64_t dV = sdesc_sw128(sKV + (2 * kb + 1) * T, 16, 1024);
+        for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+               ++bh) {  // the query heads sharing this K/V head
+          for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+            const uint32_t vbits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
+            if (leader) {
+              for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
+                const int s = it % L::kStages;
+                const uint32_t ph = (it / L::kStages) & 1u;
+                if (!mbar_wait(bars.q_full[s], ph, tmo, abort_flag) ||
+                    (gt > 0 && !mbar_wait(bar_s_ok, sfc++ & 1, tmo, abort_flag))) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                mma_ss_tile<D>(tmem + L::kColSt, dK, sdesc_sw128(sQ + s * T, 16, 1024));
+                mma_commit(bars.st_full);
+                if (gt > 0 && !mbar_wait(bar_dp_ok, dfc++ & 1, tmo, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                mma_ss_tile<D>(tmem + L::kColDPt, dV, sdesc_sw128(sDO + s * T, 16, 1024));
+                mma_commit(bars.dpt_full);
+                mma_commit(bars.q_empty[s]);
+                ++gt;
+                ++it;
+              }
+              if (!ok) fail();
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+          }
+        }
+        if (leader && ok) mma_commit(bars.kv_empty[kb]);
+      }
+      if (leader) {
+        mma_commit(bars.drain_a);
+        mbar_wait(bars.drain_a, 0, tmo, nullptr);
+      }
+      __syncwarp();
+    } else if (warp == kIssueBWarp) {
+      // ------------------------------------------------------------ dV, dK issuer
+      const bool leader = lane == 0;
+      uint32_t it = 0, prc = 0, dsc = 0;
+      bool ok = true;
+      int unit_count = 0;
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+        const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
+        const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        bool first = true;
+        for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
+               ++bh) {  // the query heads sharing this K/V head
+          for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
+            const uint32_t vbits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
+            if (leader) {
+              for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
+                const int s = it % L::kStages;
+                if (!mbar_wait(bars.p_ready, prc++ & 1, tmo, abort_flag) ||
+                    (first && unit_count > 0 &&
+                     !mbar_wait(bars.acc_free, (unit_count - 1) & 1, tmo, abort_flag))) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                mma_ts_tile<D>(tmem + L::kColDV, tmem + L::kColP, L::kPair,
+                               sdesc_sw128(sDO + s * T, 16384, 1024), !first);
+                mma_commit(bars.p_done);
+                if (!mbar_wait(bars.ds_ready, dsc++ & 1, tmo, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                mma_ts_tile<D>(tmem + L::kColDK, tmem + L::kColDS, L::kPair,
+                               sdesc_sw128(sQ + s * T, 16384, 1024), !first);
+                mma_commit(bars.ds_done);
+                mma_commit(bars.q_empty[s]);
+                first = false;
+                ++it;
+              }
+              if (!ok) fail();
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+          }
+        }
+        if (leader && ok) {
+          if (first && unit_count > 0 &&
+              !mbar_wait(bars.acc_free, (unit_count - 1) & 1, tmo, abort_flag)) {
+            ok = false;
+            fail();
+          } else {
+            mma_commit(bars.acc_full);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      if (leader) {
+        mma_commit(bars.drain_b);
+        mbar_wait(bars.drain_b, 0, tmo, nullptr);
+      }
+      __syncwarp();
     }
-    if (leader) {
-      mma_commit(bars.drain_b);
-      mbar_wait(bars.drain_b, 0, tmo, nullptr);
-    }
-    __syncwarp();
-  } else if (warp < kComputeWarps) {
+  } else {
+    regs_inc<kRegsCompute>();
     // ------------------------------------------------------------ compute
     // Warpgroup wg owns query columns [32 wg, 32 wg + 32) of every tile; the
     // thread owns one key row.
@@ -673,6 +690,11 @@ struct DqBars {
   uint32_t stall;  // test hook: never completed
 };
 
+template <int D, bool DROPOUT>
+struct DqRealloc {
+  static constexpr bool value = (D == 128) || DROPOUT;
+};
+
 template <int D, bool DROPOUT, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_split_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -680,6 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
   using L = DqL<D>;
+  // Register reallocation pays at d = 128 and with dropout (both keep more values
+  // live per compute thread); at d = 64 without dropout the compute warps need no
+  // more than the launch allocation and the kernel runs faster without it.
+  constexpr bool kRealloc = DqRealloc<D, DROPOUT>::value;
   constexpr int T = L::T;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -773,189 +799,195 @@ __global__ void __launch_bounds__(kThreads, 1)
     return jmax;
   };
 
-  if (warp == kProdWarp) {
-    // ------------------------------------------------------------ producer
-    uint32_t it = 0, k_arms = 0, v_arms = 0, qd_arms[2] = {0, 0};
-    bool ok = true;
-    int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      int bh, qt;
-      unit_coords(u, bh, qt);
-      const int kvh = kv_head(mk, bh);  // K/V head of this query head
-      const int kv_len = kv_len_of(mk, bh / mk.H);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      const int jmax = kv_limit(qt, n_kv);
-      const int qb = unit_count % L::kQDBufs, use = unit_count / L::kQDBufs;
-      if (use > 0 && !mbar_wait_warp(bars.qd_empty[qb], (use - 1) & 1, tmo, abort_flag)) {
-        fail();
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        mbar_expect_tx(bars.qd_full[qb], 2 * T);
-        tma_tile<D>(sQD + (2 * qb) * T, &tm_q, qt * kTile, bh, bars.qd_full[qb]);
-        tma_tile<D>(sQD + (2 * qb + 1) * T, &tm_do, qt * kTile, bh, bars.qd_full[qb]);
-      }
-      ++qd_arms[qb];
-      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
-        while (bits != 0u) {
-          const int j = chunk * 32 + (__ffs(bits) - 1);
-          bits &= bits - 1;
-          const int ks = it % L::kKStages, vs = it % L::kVStages;
-          if (!mbar_wait_warp(bars.k_empty[ks], ((it / L::kKStages) & 1u) ^ 1u, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            mbar_expect_tx(bars.k_full[ks], T);
-            tma_tile<D>(sK + ks * T, &tm_k, j * kTile, kvh, bars.k_full[ks]);
-          }
-          ++k_arms;
-          if (!mbar_wait_warp(bars.v_empty[vs], ((it / L::kVStages) & 1u) ^ 1u, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            mbar_expect_tx(bars.v_full[vs], T);
-            tma_tile<D>(sV + vs * T, &tm_v, j * kTile, kvh, bars.v_full[vs]);
-          }
-          ++v_arms;
-          ++it;
-        }
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < L::kKStages; ++s)
-      if (k_arms > static_cast<uint32_t>(s))
-        mbar_wait_warp(bars.k_full[s], ((k_arms - 1 - s) / L::kKStages) & 1, tmo, nullptr);
-#pragma unroll
-    for (int s = 0; s < L::kVStages; ++s)
-      if (v_arms > static_cast<uint32_t>(s))
-        mbar_wait_warp(bars.v_full[s], ((v_arms - 1 - s) / L::kVStages) & 1, tmo, nullptr);
-    for (int b = 0; b < L::kQDBufs; ++b)
-      if (qd_arms[b]) mbar_wait_warp(bars.qd_full[b], (qd_arms[b] - 1) & 1, tmo, nullptr);
-  } else if (warp == kIssueAWarp) {
-    // ------------------------------------------------------------ S, dP issuer
-    const bool leader = lane == 0;
-    uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
-    bool ok = true;
-    if (args.sync.inject_stall && leader) {
-      // Test hook: this barrier is never completed, so the bounded wait runs out.
-      if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
-        fail();
-        ok = false;
-      }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      int bh, qt;
-      unit_coords(u, bh, qt);
-      const int kv_len = kv_len_of(mk, bh / mk.H);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      const int jmax = kv_limit(qt, n_kv);
-      const int qb = unit_count % L::kQDBufs;
-      if (leader &&
-          !mbar_wait(bars.qd_full[qb], (unit_count / L::kQDBufs) & 1, tmo, abort_flag)) {
-        fail();
-        ok = false;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      const uint64_t dQ = sdesc_sw128(sQD + (2 * qb) * T, 16, 1024);
-      const uint64_t dDO = sdesc_sw128(sQD + (2 * qb + 1) * T, 16, 1024);
-      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        const uint32_t vbits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
-        if (leader) {
-          for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
-            const int ks = it % L::kKStages, vs = it % L::kVStages;
-            if (!mbar_wait(bars.k_full[ks], (it / L::kKStages) & 1u, tmo, abort_flag) ||
-                (gt > 0 && !mbar_wait(bars.s_free, sfc++ & 1, tmo, abort_flag))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            mma_ss_tile<D>(tmem + L::kColS, dQ, sdesc_sw128(sK + ks * T, 16, 1024));
-            mma_commit(bars.s_full);
-            if (!mbar_wait(bars.v_full[vs], (it / L::kVStages) & 1u, tmo, abort_flag) ||
-                (gt > 0 && !mbar_wait(bars.dp_free, dfc++ & 1, tmo, abort_flag))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            mma_ss_tile<D>(tmem + L::kColDP, dDO, sdesc_sw128(sV + vs * T, 16, 1024));
-            mma_commit(bars.dp_full);
-            mma_commit(bars.v_empty[vs]);
-            ++gt;
-            ++it;
-          }
-          if (!ok) fail();
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-      }
-      if (leader && ok) mma_commit(bars.qd_empty[qb]);
-    }
-    if (leader) {
-      mma_commit(bars.drain_a);
-      mbar_wait(bars.drain_a, 0, tmo, nullptr);
-    }
-    __syncwarp();
-  } else if (warp == kIssueBWarp) {
-    // ------------------------------------------------------------ dQ issuer
-    const bool leader = lane == 0;
-    uint32_t it = 0, dsc = 0;
-    bool ok = true;
-    int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      int bh, qt;
-      unit_coords(u, bh, qt);
-      const int kv_len = kv_len_of(mk, bh / mk.H);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      const int jmax = kv_limit(qt, n_kv);
-      bool first = true;
-      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        const uint32_t vbits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
-        if (leader) {
-          for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
-            const int ks = it % L::kKStages;
-            if (!mbar_wait(bars.ds_ready, dsc++ & 1, tmo, abort_flag) ||
-                !mbar_wait(bars.k_full[ks], (it / L::kKStages) & 1u, tmo, abort_flag) ||
-                (first && unit_count > 0 &&
-                 !mbar_wait(bars.dq_free, (unit_count - 1) & 1, tmo, abort_flag))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            mma_ts_tile<D>(tmem + L::kColDQ, tmem + L::kColDS, 16,
-                           sdesc_sw128(sK + ks * T, 16384, 1024), !first);
-            mma_commit(bars.ds_done);
-            mma_commit(bars.k_empty[ks]);
-            first = false;
-            ++it;
-          }
-          if (!ok) fail();
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-      }
-      if (leader && ok) {
-        if (first && unit_count > 0 &&
-            !mbar_wait(bars.dq_free, (unit_count - 1) & 1, tmo, abort_flag)) {
-          ok = false;
+  if (warp >= kComputeWarps) {
+    // producer, issuers and the idle warp: one warpgroup, which hands most of its
+    // registers to the compute warpgroups
+    if constexpr (kRealloc) regs_dec<kRegsAux>();
+    if (warp == kProdWarp) {
+      // ------------------------------------------------------------ producer
+      uint32_t it = 0, k_arms = 0, v_arms = 0, qd_arms[2] = {0, 0};
+      bool ok = true;
+      int unit_count = 0;
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+        int bh, qt;
+        unit_coords(u, bh, qt);
+        const int kvh = kv_head(mk, bh);  // K/V head of this query head
+        const int kv_len = kv_len_of(mk, bh / mk.H);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        const int jmax = kv_limit(qt, n_kv);
+        const int qb = unit_count % L::kQDBufs, use = unit_count / L::kQDBufs;
+        if (use > 0 && !mbar_wait_warp(bars.qd_empty[qb], (use - 1) & 1, tmo, abort_flag)) {
           fail();
-        } else {
-          mma_commit(bars.dq_full);
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_expect_tx(bars.qd_full[qb], 2 * T);
+          tma_tile<D>(sQD + (2 * qb) * T, &tm_q, qt * kTile, bh, bars.qd_full[qb]);
+          tma_tile<D>(sQD + (2 * qb + 1) * T, &tm_do, qt * kTile, bh, bars.qd_full[qb]);
+        }
+        ++qd_arms[qb];
+        for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+          uint32_t bits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
+          while (bits != 0u) {
+            const int j = chunk * 32 + (__ffs(bits) - 1);
+            bits &= bits - 1;
+            const int ks = it % L::kKStages, vs = it % L::kVStages;
+            if (!mbar_wait_warp(bars.k_empty[ks], ((it / L::kKStages) & 1u) ^ 1u, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              mbar_expect_tx(bars.k_full[ks], T);
+              tma_tile<D>(sK + ks * T, &tm_k, j * kTile, kvh, bars.k_full[ks]);
+            }
+            ++k_arms;
+            if (!mbar_wait_warp(bars.v_empty[vs], ((it / L::kVStages) & 1u) ^ 1u, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              mbar_expect_tx(bars.v_full[vs], T);
+              tma_tile<D>(sV + vs * T, &tm_v, j * kTile, kvh, bars.v_full[vs]);
+            }
+            ++v_arms;
+            ++it;
+          }
+        }
+      }
+  #pragma unroll
+      for (int s = 0; s < L::kKStages; ++s)
+        if (k_arms > static_cast<uint32_t>(s))
+          mbar_wait_warp(bars.k_full[s], ((k_arms - 1 - s) / L::kKStages) & 1, tmo, nullptr);
+  #pragma unroll
+      for (int s = 0; s < L::kVStages; ++s)
+        if (v_arms > static_cast<uint32_t>(s))
+          mbar_wait_warp(bars.v_full[s], ((v_arms - 1 - s) / L::kVStages) & 1, tmo, nullptr);
+      for (int b = 0; b < L::kQDBufs; ++b)
+        if (qd_arms[b]) mbar_wait_warp(bars.qd_full[b], (qd_arms[b] - 1) & 1, tmo, nullptr);
+    } else if (warp == kIssueAWarp) {
+      // ------------------------------------------------------------ S, dP issuer
+      const bool leader = lane == 0;
+      uint32_t it = 0, gt = 0, sfc = 0, dfc = 0;
+      bool ok = true;
+      if (args.sync.inject_stall && leader) {
+        // Test hook: this barrier is never completed, so the bounded wait runs out.
+        if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
+          fail();
+          ok = false;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      int unit_count = 0;
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+        int bh, qt;
+        unit_coords(u, bh, qt);
+        const int kv_len = kv_len_of(mk, bh / mk.H);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        const int jmax = kv_limit(qt, n_kv);
+        const int qb = unit_count % L::kQDBufs;
+        if (leader &&
+            !mbar_wait(bars.qd_full[qb], (unit_count / L::kQDBufs) & 1, tmo, abort_flag)) {
+          fail();
+          ok = false;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        const uint64_t dQ = sdesc_sw128(sQD + (2 * qb) * T, 16, 1024);
+        const uint64_t dDO = sdesc_sw128(sQD + (2 * qb + 1) * T, 16, 1024);
+        for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+          const uint32_t vbits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
+          if (leader) {
+            for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
+              const int ks = it % L::kKStages, vs = it % L::kVStages;
+              if (!mbar_wait(bars.k_full[ks], (it / L::kKStages) & 1u, tmo, abort_flag) ||
+                  (gt > 0 && !mbar_wait(bars.s_free, sfc++ & 1, tmo, abort_flag))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_ss_tile<D>(tmem + L::kColS, dQ, sdesc_sw128(sK + ks * T, 16, 1024));
+              mma_commit(bars.s_full);
+              if (!mbar_wait(bars.v_full[vs], (it / L::kVStages) & 1u, tmo, abort_flag) ||
+                  (gt > 0 && !mbar_wait(bars.dp_free, dfc++ & 1, tmo, abort_flag))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_ss_tile<D>(tmem + L::kColDP, dDO, sdesc_sw128(sV + vs * T, 16, 1024));
+              mma_commit(bars.dp_full);
+              mma_commit(bars.v_empty[vs]);
+              ++gt;
+              ++it;
+            }
+            if (!ok) fail();
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        if (leader && ok) mma_commit(bars.qd_empty[qb]);
+      }
+      if (leader) {
+        mma_commit(bars.drain_a);
+        mbar_wait(bars.drain_a, 0, tmo, nullptr);
+      }
+      __syncwarp();
+    } else if (warp == kIssueBWarp) {
+      // ------------------------------------------------------------ dQ issuer
+      const bool leader = lane == 0;
+      uint32_t it = 0, dsc = 0;
+      bool ok = true;
+      int unit_count = 0;
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+        int bh, qt;
+        unit_coords(u, bh, qt);
+        const int kv_len = kv_len_of(mk, bh / mk.H);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        const int jmax = kv_limit(qt, n_kv);
+        bool first = true;
+        for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+          const uint32_t vbits = warp_valid_bits<WIN>(mk, qt, chunk, n_q, n_kv);
+          if (leader) {
+            for (uint32_t bits = vbits; bits != 0u && ok; bits &= bits - 1) {
+              const int ks = it % L::kKStages;
+              if (!mbar_wait(bars.ds_ready, dsc++ & 1, tmo, abort_flag) ||
+                  !mbar_wait(bars.k_full[ks], (it / L::kKStages) & 1u, tmo, abort_flag) ||
+                  (first && unit_count > 0 &&
+                   !mbar_wait(bars.dq_free, (unit_count - 1) & 1, tmo, abort_flag))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_ts_tile<D>(tmem + L::kColDQ, tmem + L::kColDS, 16,
+                             sdesc_sw128(sK + ks * T, 16384, 1024), !first);
+              mma_commit(bars.ds_done);
+              mma_commit(bars.k_empty[ks]);
+              first = false;
+              ++it;
+            }
+            if (!ok) fail();
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        if (leader && ok) {
+          if (first && unit_count > 0 &&
+              !mbar_wait(bars.dq_free, (unit_count - 1) & 1, tmo, abort_flag)) {
+            ok = false;
+            fail();
+          } else {
+            mma_commit(bars.dq_full);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      if (leader) {
+        mma_commit(bars.drain_b);
+        mbar_wait(bars.drain_b, 0, tmo, nullptr);
+      }
+      __syncwarp();
     }
-    if (leader) {
-      mma_commit(bars.drain_b);
-      mbar_wait(bars.drain_b, 0, tmo, nullptr);
-    }
-    __syncwarp();
-  } else if (warp < kComputeWarps) {
+  } else {
+    if constexpr (kRealloc) regs_inc<kRegsCompute>();
     // ------------------------------------------------------------ compute
     // Warpgroup wg owns key columns [32 wg, 32 wg + 32) of every tile; the
     // thread owns one query row.
@@ -1167,8 +1199,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Shared-memory opt-in, and a check that the kernel was built for the
+// register count its in-kernel reallocation assumes: launched with fewer
+// registers per thread, the compute warpgroups' increase could never be granted
+// and would wait forever, so such a kernel is refused instead of launched.
 template <typename K>
-cudaError_t set_smem_split(K kern, int bytes) {
+cudaError_t set_smem_split(K kern, int bytes, bool realloc) {
+  if (realloc) {
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs < kRegsLaunch || attr.maxThreadsPerBlock < kThreads)
+      return cudaErrorInvalidConfiguration;
+  }
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
@@ -1185,7 +1228,7 @@ cudaError_t launch_dkdv_split_d(const CUtensorMap& tq, const CUtensorMap& tk,
                       : fa_bwd_dkdv_split_kernel<D, DR, false, false>);
   };
   auto kern = dropout ? pick(std::true_type{}) : pick(std::false_type{});
-  cudaError_t e = set_smem_split(kern, DkdvL<D>::kSmemBytes);
+  cudaError_t e = set_smem_split(kern, DkdvL<D>::kSmemBytes, true);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, DkdvL<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
@@ -1200,7 +1243,8 @@ cudaError_t launch_dq_split_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
                              : fa_bwd_dq_split_kernel<D, true, false>)
                       : (win ? fa_bwd_dq_split_kernel<D, false, true>
                              : fa_bwd_dq_split_kernel<D, false, false>);
-  cudaError_t e = set_smem_split(kern, DqL<D>::kSmemBytes);
+  const bool realloc = dropout ? DqRealloc<D, true>::value : DqRealloc<D, false>::value;
+  cudaError_t e = set_smem_split(kern, DqL<D>::kSmemBytes, realloc);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, DqL<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();

@@ -35,10 +35,22 @@ namespace fa {
 
 namespace {
 
-constexpr int kFwdThreads = 352;
+constexpr int kSoftmaxWarps = 8;  // two warpgroups, one per query tile
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kPvWarp = 10;  // second MMA issuer (decoupled schedule)
+// Warp 11 idles: it completes the third warpgroup, since registers move between
+// whole warpgroups.
+constexpr int kFwdThreads = 12 * 32;
+// Registers per thread: 168 at launch (three warps per sub-partition); the
+// producer and issuer warpgroup gives part of its share to the softmax warps,
+// which hold a 128-score row and its packed probabilities.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsAux = 96;
+static_assert(kSoftmaxWarps * 32 * kRegsSoftmax + (kFwdThreads - kSoftmaxWarps * 32) * kRegsAux <=
+                  kFwdThreads * kRegsLaunch,
+              "register reallocation exceeds the block's launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when m grows by > 2^8
 
 template <int D>
@@ -192,280 +204,138 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t sK = smem_u32(smem + L::kKOff);
   const uint32_t sV = smem_u32(smem + L::kVOff);
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    uint32_t it = 0;          // K/V ring position (running over all units)
-    uint32_t k_arms = 0, v_arms = 0;  // loads issued into the K / V rings
-    uint32_t q_armed = 0;
-    bool ok = true;
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-    }
-    int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
-      const int kvh = kv_head(mk, uc.bh);  // K/V head of this query head
-      const int kv_len = kv_len_of(mk, uc.b);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      int jmax = n_kv;
-      if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
-      if (unit_count > 0) {
-        if (!mbar_wait_warp(bars.q_empty, (unit_count - 1) & 1, tmo, abort_flag)) {
-          fail();
-          ok = false;
-          break;
-        }
-      }
+  if (warp >= kSoftmaxWarps) {
+    // producer, issuers and the idle warp: one warpgroup, which hands most of its
+    // registers to the softmax warpgroups
+    regs_dec<kRegsAux>();
+    if (warp == kProducerWarp) {
+      // ------------------------------------------------------------ producer
+      uint32_t it = 0;          // K/V ring position (running over all units)
+      uint32_t k_arms = 0, v_arms = 0;  // loads issued into the K / V rings
+      uint32_t q_armed = 0;
+      bool ok = true;
       if (lane == 0) {
-        for (int x = 0; x < 2; ++x) {
-          mbar_expect_tx(bars.q_full[x], L::kTileBytes);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(sQ + x * L::kTileBytes + c * 16384, &tm_q, c * 64, (uc.qt0 + x) * kTile,
-                        uc.bh, bars.q_full[x]);
-        }
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
       }
-      ++q_armed;
-      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        uint32_t bits = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv) |
-                        warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
-        while (bits != 0u) {
-          const int j = chunk * 32 + (__ffs(bits) - 1);
-          bits &= bits - 1;
-          const int s = it % L::kStages;
-          const uint32_t ph = (it / L::kStages) & 1u;
-          if (!mbar_wait_warp(bars.k_empty[s], ph ^ 1u, tmo, abort_flag)) {
+      int unit_count = 0;
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+        const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
+        const int kvh = kv_head(mk, uc.bh);  // K/V head of this query head
+        const int kv_len = kv_len_of(mk, uc.b);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        int jmax = n_kv;
+        if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
+        if (unit_count > 0) {
+          if (!mbar_wait_warp(bars.q_empty, (unit_count - 1) & 1, tmo, abort_flag)) {
             fail();
             ok = false;
             break;
           }
-          if (lane == 0) {
-            mbar_expect_tx(bars.k_full[s], L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(sK + s * L::kTileBytes + c * 16384, &tm_k, c * 64, j * kTile, kvh,
-                          bars.k_full[s]);
-          }
-          ++k_arms;
-          if (!mbar_wait_warp(bars.v_empty[s], ph ^ 1u, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            mbar_expect_tx(bars.v_full[s], L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(sV + s * L::kTileBytes + c * 16384, &tm_v, c * 64, j * kTile, kvh,
-                          bars.v_full[s]);
-          }
-          ++v_arms;
-          ++it;
         }
-      }
-    }
-    // Drain: every load this warp issued must land before the CTA exits.
-    // Stage s was armed for ring positions s, s + S, ...; wait for the last one.
-#pragma unroll
-    for (int s = 0; s < L::kStages; ++s) {
-      if (k_arms > static_cast<uint32_t>(s))
-        mbar_wait_warp(bars.k_full[s], ((k_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
-      if (v_arms > static_cast<uint32_t>(s))
-        mbar_wait_warp(bars.v_full[s], ((v_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
-    }
-    if (q_armed) {
-      mbar_wait_warp(bars.q_full[0], (q_armed - 1) & 1, tmo, nullptr);
-      mbar_wait_warp(bars.q_full[1], (q_armed - 1) & 1, tmo, nullptr);
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // Lane 0 alone waits and issues: tcgen05.mma issue blocks while the tensor
-    // core is busy (its queue is shallow), so every cycle this thread spends on
-    // anything else is a tensor-core bubble. The rest of the warp only helps
-    // evaluate the tile lists (one ballot per 32 key tiles).
-    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
-    constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);   // O += P V, V MN-major
-    constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
-    const bool leader = (lane == 0);
-    const uint64_t dQa = sdesc_sw128(sQ, 16, 1024);
-    const uint64_t dQb = sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
-    const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
-    const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
-    uint32_t it = 0;
-    uint32_t p_cnt0 = 0, p_cnt1 = 0, sf_cnt0 = 0, sf_cnt1 = 0;
-    bool s_seen0 = false, s_seen1 = false;
-    bool ok = true;
-    if (args.sync.inject_stall && leader) {
-      // Test hook: this barrier is never completed, so the bounded wait runs out.
-      if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
-        fail();
-        ok = false;
-      }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    auto issue_S = [&](int x, int s) {
-      const uint64_t dq = x ? dQb : dQa;
-      const uint64_t dk = dK0 + static_cast<uint64_t>(s) * kStageStep;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-        mma_ss(tmem + L::col_s(x), dq + off, dk + off, kIdS, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(bars.s_full[x]);
-    };
-    auto issue_PV = [&](int x, int s, bool first) {
-      const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
-               dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
-               (first && kk == 0) ? 0u : 1u);
-    };
-    int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-      const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
-      const int kv_len = kv_len_of(mk, uc.b);
-      const int n_kv = (kv_len + kTile - 1) / kTile;
-      int jmax = n_kv;
-      if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
-      const uint32_t uph = unit_count & 1;
-      bool pend0 = false, pend1 = false, first0 = true, first1 = true;
-      int prev_stage = -1;
-      uint32_t prev_ph = 0;
-      // PV of query tile x for the tile S-issued at the previous ring position.
-      auto pv = [&](int x) -> bool {
-        uint32_t& pc = x ? p_cnt1 : p_cnt0;
-        bool& first = x ? first1 : first0;
-        if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
-        ++pc;
-        if (first && unit_count > 0 &&
-            !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
-          return false;
-        tc_fence_after();
-        issue_PV(x, prev_stage, first);
-        if constexpr (L::kSepP) mma_commit(bars.pv_done[x]);
-        first = false;
-        return true;
-      };
-      if (leader) {
-        ok = mbar_wait(bars.q_full[0], uph, tmo, abort_flag) &&
-             mbar_wait(bars.q_full[1], uph, tmo, abort_flag);
-        if (!ok) fail();
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-        const uint32_t va = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv);
-        const uint32_t vb = warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
-        if (leader) {
-          uint32_t bits = va | vb;
-          while (bits != 0u && ok) {
-            const int bit = __ffs(bits) - 1;
+        if (lane == 0) {
+          for (int x = 0; x < 2; ++x) {
+            mbar_expect_tx(bars.q_full[x], L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_3d(sQ + x * L::kTileBytes + c * 16384, &tm_q, c * 64, (uc.qt0 + x) * kTile,
+                          uc.bh, bars.q_full[x]);
+          }
+        }
+        ++q_armed;
+        for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+          uint32_t bits = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv) |
+                          warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
+          while (bits != 0u) {
+            const int j = chunk * 32 + (__ffs(bits) - 1);
             bits &= bits - 1;
-            const bool v0 = ((va >> bit) & 1u) != 0u, v1 = ((vb >> bit) & 1u) != 0u;
             const int s = it % L::kStages;
             const uint32_t ph = (it / L::kStages) & 1u;
-            if (!mbar_wait(bars.k_full[s], ph, tmo, abort_flag)) {
+            if (!mbar_wait_warp(bars.k_empty[s], ph ^ 1u, tmo, abort_flag)) {
+              fail();
               ok = false;
               break;
             }
-            if constexpr (L::kSepP) {
-              // S of this position as soon as the softmax has read the previous S ...
-              if (v0) {
-                if (s_seen0 && !mbar_wait(bars.s_free[0], sf_cnt0++ & 1, tmo, abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                issue_S(0, s);
-                s_seen0 = true;
-              }
-              if (v1) {
-                if (s_seen1 && !mbar_wait(bars.s_free[1], sf_cnt1++ & 1, tmo, abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                issue_S(1, s);
-                s_seen1 = true;
-              }
-              // (the PVs come from the PV-issuer warp)
-            } else {
-              // P is written over S: PV of the previous tile of x must be issued
-              // before the next S of x.
-              if (prev_stage >= 0 &&
-                  !mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag)) {
-                ok = false;
-                break;
-              }
-              const bool had_pv = pend0 || pend1;
-              if (pend0 && !pv(0)) {
-                ok = false;
-                break;
-              }
-              if (v0) issue_S(0, s);
-              if (pend1 && !pv(1)) {
-                ok = false;
-                break;
-              }
-              if (v1) issue_S(1, s);
-              if (had_pv) mma_commit(bars.v_empty[prev_stage]);
+            if (lane == 0) {
+              mbar_expect_tx(bars.k_full[s], L::kTileBytes);
+              for (int c = 0; c < L::kChunks; ++c)
+                tma_load_3d(sK + s * L::kTileBytes + c * 16384, &tm_k, c * 64, j * kTile, kvh,
+                            bars.k_full[s]);
             }
-            mma_commit(bars.k_empty[s]);
-            pend0 = v0;
-            pend1 = v1;
-            prev_stage = s;
-            prev_ph = ph;
+            ++k_arms;
+            if (!mbar_wait_warp(bars.v_empty[s], ph ^ 1u, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              mbar_expect_tx(bars.v_full[s], L::kTileBytes);
+              for (int c = 0; c < L::kChunks; ++c)
+                tma_load_3d(sV + s * L::kTileBytes + c * 16384, &tm_v, c * 64, j * kTile, kvh,
+                            bars.v_full[s]);
+            }
+            ++v_arms;
             ++it;
           }
-          if (!ok) fail();
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      if (leader && ok && L::kSepP) {
-        mma_commit(bars.q_empty);
-      } else if (leader && ok) {
-        // Flush the PVs of the last position, then release it.
-        if (prev_stage >= 0) {
-          ok = mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag) &&
-               (!pend0 || pv(0)) && (!pend1 || pv(1));
-          if (ok) mma_commit(bars.v_empty[prev_stage]);
-        }
-        // A query tile without PV in this unit still consumes the epilogue
-        // handshake of the previous unit.
-        if (ok && first0 && unit_count > 0)
-          ok = mbar_wait(bars.o_free[0], (unit_count - 1) & 1, tmo, abort_flag);
-        if (ok && first1 && unit_count > 0)
-          ok = mbar_wait(bars.o_free[1], (unit_count - 1) & 1, tmo, abort_flag);
-        if (ok) {
-          if constexpr (!L::kSepP) {
-            mma_commit(bars.o_full[0]);
-            mma_commit(bars.o_full[1]);
-          }
-          mma_commit(bars.q_empty);
-        } else {
+      // Drain: every load this warp issued must land before the CTA exits.
+      // Stage s was armed for ring positions s, s + S, ...; wait for the last one.
+  #pragma unroll
+      for (int s = 0; s < L::kStages; ++s) {
+        if (k_arms > static_cast<uint32_t>(s))
+          mbar_wait_warp(bars.k_full[s], ((k_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
+        if (v_arms > static_cast<uint32_t>(s))
+          mbar_wait_warp(bars.v_full[s], ((v_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
+      }
+      if (q_armed) {
+        mbar_wait_warp(bars.q_full[0], (q_armed - 1) & 1, tmo, nullptr);
+        mbar_wait_warp(bars.q_full[1], (q_armed - 1) & 1, tmo, nullptr);
+      }
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
+      // Lane 0 alone waits and issues: tcgen05.mma issue blocks while the tensor
+      // core is busy (its queue is shallow), so every cycle this thread spends on
+      // anything else is a tensor-core bubble. The rest of the warp only helps
+      // evaluate the tile lists (one ballot per 32 key tiles).
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);   // O += P V, V MN-major
+      constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
+      const bool leader = (lane == 0);
+      const uint64_t dQa = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dQb = sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
+      uint32_t it = 0;
+      uint32_t p_cnt0 = 0, p_cnt1 = 0, sf_cnt0 = 0, sf_cnt1 = 0;
+      bool s_seen0 = false, s_seen1 = false;
+      bool ok = true;
+      if (args.sync.inject_stall && leader) {
+        // Test hook: this barrier is never completed, so the bounded wait runs out.
+        if (!mbar_wait(bars.stall, 0, tmo, abort_flag)) {
           fail();
+          ok = false;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-    }
-    // Drain: all issued MMAs must finish before tensor memory is released.
-    if (leader) {
-      mma_commit(bars.drain);
-      mbar_wait(bars.drain, 0, tmo, nullptr);
-    }
-    __syncwarp();
-  } else if (warp == kPvWarp) {
-    // ------------------------------------------------------------ PV issuer
-    // Decoupled schedule only: O_x += P_x V_j as soon as P_x of key tile j is
-    // ready, from a second issuing thread, so that the tensor core keeps
-    // receiving work while the S issuer waits on its own barriers. Its MMAs are
-    // tracked by its own commits (pv_done, v_empty).
-    if constexpr (L::kSepP) {
-      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);
-      constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
-      const bool leader = (lane == 0);
-      const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
-      uint32_t it = 0, p_cnt0 = 0, p_cnt1 = 0;
-      bool ok = true;
+      auto issue_S = [&](int x, int s) {
+        const uint64_t dq = x ? dQb : dQa;
+        const uint64_t dk = dK0 + static_cast<uint64_t>(s) * kStageStep;
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + L::col_s(x), dq + off, dk + off, kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bars.s_full[x]);
+      };
+      auto issue_PV = [&](int x, int s, bool first) {
+        const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
+  #pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
+                 dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
+                 (first && kk == 0) ? 0u : 1u);
+      };
       int unit_count = 0;
       for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
         const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
@@ -473,8 +343,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int n_kv = (kv_len + kTile - 1) / kTile;
         int jmax = n_kv;
         if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
-        bool first0 = true, first1 = true;
-        auto pv = [&](int x, int s) -> bool {
+        const uint32_t uph = unit_count & 1;
+        bool pend0 = false, pend1 = false, first0 = true, first1 = true;
+        int prev_stage = -1;
+        uint32_t prev_ph = 0;
+        // PV of query tile x for the tile S-issued at the previous ring position.
+        auto pv = [&](int x) -> bool {
           uint32_t& pc = x ? p_cnt1 : p_cnt0;
           bool& first = x ? first1 : first0;
           if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
@@ -483,16 +357,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
             return false;
           tc_fence_after();
-          const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
-                   dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
-                   (first && kk == 0) ? 0u : 1u);
-          mma_commit(bars.pv_done[x]);
+          issue_PV(x, prev_stage, first);
+          if constexpr (L::kSepP) mma_commit(bars.pv_done[x]);
           first = false;
           return true;
         };
+        if (leader) {
+          ok = mbar_wait(bars.q_full[0], uph, tmo, abort_flag) &&
+               mbar_wait(bars.q_full[1], uph, tmo, abort_flag);
+          if (!ok) fail();
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
           const uint32_t va = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv);
           const uint32_t vb = warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
@@ -501,38 +376,181 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             while (bits != 0u && ok) {
               const int bit = __ffs(bits) - 1;
               bits &= bits - 1;
+              const bool v0 = ((va >> bit) & 1u) != 0u, v1 = ((vb >> bit) & 1u) != 0u;
               const int s = it % L::kStages;
               const uint32_t ph = (it / L::kStages) & 1u;
-              if (!mbar_wait(bars.v_full[s], ph, tmo, abort_flag) ||
-                  (((va >> bit) & 1u) && !pv(0, s)) || (((vb >> bit) & 1u) && !pv(1, s))) {
+              if (!mbar_wait(bars.k_full[s], ph, tmo, abort_flag)) {
                 ok = false;
                 break;
               }
-              mma_commit(bars.v_empty[s]);
+              if constexpr (L::kSepP) {
+                // S of this position as soon as the softmax has read the previous S ...
+                if (v0) {
+                  if (s_seen0 && !mbar_wait(bars.s_free[0], sf_cnt0++ & 1, tmo, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  issue_S(0, s);
+                  s_seen0 = true;
+                }
+                if (v1) {
+                  if (s_seen1 && !mbar_wait(bars.s_free[1], sf_cnt1++ & 1, tmo, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  issue_S(1, s);
+                  s_seen1 = true;
+                }
+                // (the PVs come from the PV-issuer warp)
+              } else {
+                // P is written over S: PV of the previous tile of x must be issued
+                // before the next S of x.
+                if (prev_stage >= 0 &&
+                    !mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                const bool had_pv = pend0 || pend1;
+                if (pend0 && !pv(0)) {
+                  ok = false;
+                  break;
+                }
+                if (v0) issue_S(0, s);
+                if (pend1 && !pv(1)) {
+                  ok = false;
+                  break;
+                }
+                if (v1) issue_S(1, s);
+                if (had_pv) mma_commit(bars.v_empty[prev_stage]);
+              }
+              mma_commit(bars.k_empty[s]);
+              pend0 = v0;
+              pend1 = v1;
+              prev_stage = s;
+              prev_ph = ph;
               ++it;
             }
             if (!ok) fail();
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        if (leader && ok) {
+        if (leader && ok && L::kSepP) {
+          mma_commit(bars.q_empty);
+        } else if (leader && ok) {
+          // Flush the PVs of the last position, then release it.
+          if (prev_stage >= 0) {
+            ok = mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag) &&
+                 (!pend0 || pv(0)) && (!pend1 || pv(1));
+            if (ok) mma_commit(bars.v_empty[prev_stage]);
+          }
           // A query tile without PV in this unit still consumes the epilogue
           // handshake of the previous unit.
-          if (first0 && unit_count > 0)
+          if (ok && first0 && unit_count > 0)
             ok = mbar_wait(bars.o_free[0], (unit_count - 1) & 1, tmo, abort_flag);
           if (ok && first1 && unit_count > 0)
             ok = mbar_wait(bars.o_free[1], (unit_count - 1) & 1, tmo, abort_flag);
-          if (!ok) fail();
+          if (ok) {
+            if constexpr (!L::kSepP) {
+              mma_commit(bars.o_full[0]);
+              mma_commit(bars.o_full[1]);
+            }
+            mma_commit(bars.q_empty);
+          } else {
+            fail();
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
+      // Drain: all issued MMAs must finish before tensor memory is released.
       if (leader) {
-        mma_commit(bars.drain2);
-        mbar_wait(bars.drain2, 0, tmo, nullptr);
+        mma_commit(bars.drain);
+        mbar_wait(bars.drain, 0, tmo, nullptr);
       }
       __syncwarp();
+    } else if (warp == kPvWarp) {
+      // ------------------------------------------------------------ PV issuer
+      // Decoupled schedule only: O_x += P_x V_j as soon as P_x of key tile j is
+      // ready, from a second issuing thread, so that the tensor core keeps
+      // receiving work while the S issuer waits on its own barriers. Its MMAs are
+      // tracked by its own commits (pv_done, v_empty).
+      if constexpr (L::kSepP) {
+        constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);
+        constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
+        const bool leader = (lane == 0);
+        const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
+        uint32_t it = 0, p_cnt0 = 0, p_cnt1 = 0;
+        bool ok = true;
+        int unit_count = 0;
+        for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+          const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
+          const int kv_len = kv_len_of(mk, uc.b);
+          const int n_kv = (kv_len + kTile - 1) / kTile;
+          int jmax = n_kv;
+          if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
+          bool first0 = true, first1 = true;
+          auto pv = [&](int x, int s) -> bool {
+            uint32_t& pc = x ? p_cnt1 : p_cnt0;
+            bool& first = x ? first1 : first0;
+            if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
+            ++pc;
+            if (first && unit_count > 0 &&
+                !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
+              return false;
+            tc_fence_after();
+            const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
+  #pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
+                     dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
+                     (first && kk == 0) ? 0u : 1u);
+            mma_commit(bars.pv_done[x]);
+            first = false;
+            return true;
+          };
+          for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+            const uint32_t va = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv);
+            const uint32_t vb = warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
+            if (leader) {
+              uint32_t bits = va | vb;
+              while (bits != 0u && ok) {
+                const int bit = __ffs(bits) - 1;
+                bits &= bits - 1;
+                const int s = it % L::kStages;
+                const uint32_t ph = (it / L::kStages) & 1u;
+                if (!mbar_wait(bars.v_full[s], ph, tmo, abort_flag) ||
+                    (((va >> bit) & 1u) && !pv(0, s)) || (((vb >> bit) & 1u) && !pv(1, s))) {
+                  ok = false;
+                  break;
+                }
+                mma_commit(bars.v_empty[s]);
+                ++it;
+              }
+              if (!ok) fail();
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+          }
+          if (leader && ok) {
+            // A query tile without PV in this unit still consumes the epilogue
+            // handshake of the previous unit.
+            if (first0 && unit_count > 0)
+              ok = mbar_wait(bars.o_free[0], (unit_count - 1) & 1, tmo, abort_flag);
+            if (ok && first1 && unit_count > 0)
+              ok = mbar_wait(bars.o_free[1], (unit_count - 1) & 1, tmo, abort_flag);
+            if (!ok) fail();
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        if (leader) {
+          mma_commit(bars.drain2);
+          mbar_wait(bars.drain2, 0, tmo, nullptr);
+        }
+        __syncwarp();
+      }
     }
   } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int x = warp >> 2;                 // query tile within the unit (0 = a, 1 = b)
     const int quad = warp & 3;               // tensor-memory lane quadrant of this warp
@@ -792,8 +810,15 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
   using L = FwdLayout<D>;
   const bool win = a.mask.wl >= 0 || a.mask.wr >= 0;
   auto kern = win ? fa_fwd_kernel<D, DROPOUT, true> : fa_fwd_kernel<D, DROPOUT, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kSmemBytes);
+  // The in-kernel register reallocation assumes kRegsLaunch registers per thread
+  // at launch: with fewer, the softmax warpgroups' increase could never be
+  // granted and would wait forever, so such a kernel is refused.
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs < kRegsLaunch || attr.maxThreadsPerBlock < kFwdThreads)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, kFwdThreads, L::kSmemBytes, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();

@@ -74,6 +74,20 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
   return __all_sync(0xffffffffu, ok);
 }
 
+// ---------------------------------------------------------------- registers
+// Moves registers between warpgroups: every warp of a warpgroup executes the
+// same call. An increase waits until the block's pool (its threads times the
+// per-thread count it was launched with) has the registers free, so the
+// requests of all warpgroups must add up to at most that pool.
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 // 3-D tiled tensor load (coordinates innermost first) completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
