@@ -19,9 +19,9 @@ pytestmark = pytest.mark.gpu
 SAMPLED = {
     "gpt2_medium": [(0, 0), (63, 15), (17, 9)],
     "causal_4k": [(0, 0), (7, 31)],
-    "long_16k_d64": [(0, 15)],
-    "long_16k_d128": [(0, 15)],
-    "butterfly_16k": [(3, 15)],
+    "long_16k_d64": [(0, 0), (0, 15)],
+    "long_16k_d128": [(0, 0), (0, 15)],
+    "butterfly_16k": [(0, 0), (3, 15)],
     "gqa_causal_4k": [(7, 31)],
     "sliding_16k": [(1, 31)],
 }
