@@ -24,9 +24,10 @@ namespace fa {
 
 namespace {
 
-constexpr int kBwdThreads = 320;
-constexpr int kProducerWarp = 8;
+constexpr int kBwdThreads = 352;
+constexpr int kProducerWarp = 8;    // K, V and the Q ring (with lse)
 constexpr int kMmaWarp = 9;
+constexpr int kDOProducerWarp = 10; // the dO ring (with D)
 
 // ------------------------------------------------------------------ preprocess
 // D = rowsum(dO * O) in fp32; 8 threads per row, 16-byte loads.
@@ -73,31 +74,39 @@ __device__ __forceinline__ float lse2_of(const float* lse, long long idx, bool i
 // ================================================================== dK, dV
 // One work unit = one (b, h) head and one 128-row key tile (K_j, V_j stay in
 // shared memory); the loop runs over the query tiles that may attend to it.
-//   warp 8      TMA producer: K_j, V_j per unit; Q_i, dO_i (and lse_i, D_i via
-//               plain loads) through an NS-stage ring.
+//   warp 8      TMA producer: K_j, V_j per unit; Q_i (and lse_i via plain
+//               loads) through the Q ring.
+//   warp 10     TMA producer: dO_i (and D_i via plain loads) through the dO ring.
 //   warp 9      MMA issuer: S^T = K Q^T, dP^T = V dO^T (shared-memory
 //               operands), dV += P^T dO and dK += dS^T Q (A from tensor memory).
 //   warps 0-7   two warpgroups, each owning 64 of the 128 query columns of
 //               every tile (thread = key row): P^T = exp2(S^T c - lse2),
 //               dropout, dS^T = P^T (Z dP^T / (1-p) - D); P^T and dS^T go back
 //               to tensor memory as bf16 over the columns they were read from.
+// A Q tile is last read by dK of the step after its own, a dO tile by dV of its
+// own step, so the Q ring is one stage deeper than the dO ring (the dropout
+// instances keep two Q stages to leave room for their Philox scratch).
 // Tensor memory: dV [0, d), dK [d, 2d), S^T [2d, 2d+128), dP^T [2d+128, 2d+256).
-template <int D>
+template <int D, bool DROPOUT>
 struct DkdvLayout {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kQStages = DROPOUT ? 2 : 3;
+  static constexpr int kDOStages = 2;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
   static constexpr int kQOff = 2 * kTileBytes;
-  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kLseOff = kDOOff + kStages * kTileBytes;      // kStages x 128 fp32
-  static constexpr int kDsumOff = kLseOff + kStages * 512;          // kStages x 128 fp32
-  static constexpr int kDropOff = kDsumOff + kStages * 512;         // 8 warps x 2 KB Philox scratch
-  static constexpr int kBarOff = kDropOff + 8 * 2048;
-  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 2;
+  static constexpr int kDOOff = kQOff + kQStages * kTileBytes;
+  static constexpr int kLseOff = kDOOff + kDOStages * kTileBytes;  // kQStages x 128 fp32
+  static constexpr int kDsumOff = kLseOff + kQStages * 512;        // kDOStages x 128 fp32
+  static constexpr int kDropOff = kDsumOff + kDOStages * 512;      // 8 warps x 2 KB Philox scratch
+  static constexpr int kBarOff = kDropOff + (DROPOUT ? 8 * 2048 : 0);
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDOStages + 6 + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+  // No slack for rounding the base up: the kernel checks that the dynamic
+  // shared memory starts on a 1024-byte boundary (the SW128 tiles need it).
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static_assert(kSmemBytes <= 232448, "d=128 dK/dV layout exceeds 227 KB of shared memory");
   __device__ static constexpr uint32_t col_dv() { return 0u; }
   __device__ static constexpr uint32_t col_dk() { return static_cast<uint32_t>(D); }
   __device__ static constexpr uint32_t col_st() { return static_cast<uint32_t>(2 * D); }
@@ -110,10 +119,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do, const BwdArgs args) {
-  using L = DkdvLayout<D>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  using L = DkdvLayout<D, DROPOUT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0u) {  // uniform over the block: nothing has started yet
+    if (threadIdx.x == 0) record_error(args.sync.status, kStatusCuda);
+    return;
+  }
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -129,15 +140,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* lse_s = reinterpret_cast<float*>(smem + L::kLseOff);
   float* dsum_s = reinterpret_cast<float*>(smem + L::kDsumOff);
 
-  uint32_t b_kv_full, b_kv_empty, b_q_full[4], b_q_empty[4], b_st_full, b_dpt_full, b_p_ready,
-      b_ds_ready, b_acc_full, b_acc_free, b_drain, b_stall;
+  // ring barriers by stage: full, then empty, Q ring first
+  const uint32_t bar0 = smem_u32(bar_mem);
+  auto q_full = [&](int s) { return bar0 + 8u * static_cast<uint32_t>(2 + s); };
+  auto q_empty = [&](int s) { return bar0 + 8u * static_cast<uint32_t>(2 + L::kQStages + s); };
+  auto do_full = [&](int s) {
+    return bar0 + 8u * static_cast<uint32_t>(2 + 2 * L::kQStages + s);
+  };
+  auto do_empty = [&](int s) {
+    return bar0 + 8u * static_cast<uint32_t>(2 + 2 * L::kQStages + L::kDOStages + s);
+  };
+  uint32_t b_kv_full, b_kv_empty, b_st_full, b_dpt_full, b_p_ready, b_ds_ready, b_acc_full,
+      b_acc_free, b_drain, b_stall;
   {
     int i = 0;
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
     b_kv_full = nb();
     b_kv_empty = nb();
-    for (int s = 0; s < L::kStages; ++s) b_q_full[s] = nb();
-    for (int s = 0; s < L::kStages; ++s) b_q_empty[s] = nb();
+    i += 2 * (L::kQStages + L::kDOStages);
     b_st_full = nb();
     b_dpt_full = nb();
     b_p_ready = nb();
@@ -151,9 +171,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *abort_flag = 0;
     mbar_init(b_kv_full, 1);
     mbar_init(b_kv_empty, 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(b_q_full[s], 32);
-      mbar_init(b_q_empty[s], 1 + 8);
+    // full: the 32 producer lanes (lse / D staged by plain stores, one lane
+    // also arms the TMA bytes); empty: the MMA commit after the tile's last
+    // contraction and one lane of each compute warp once lse / D are read
+    for (int s = 0; s < L::kQStages; ++s) {
+      mbar_init(q_full(s), 32);
+      mbar_init(q_empty(s), 1 + 8);
+    }
+    for (int s = 0; s < L::kDOStages; ++s) {
+      mbar_init(do_full(s), 32);
+      mbar_init(do_empty(s), 1 + 8);
     }
     mbar_init(b_st_full, 1);
     mbar_init(b_dpt_full, 1);
@@ -183,9 +210,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::kQOff);
   const uint32_t sDO = smem_u32(smem + L::kDOOff);
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    uint32_t it = 0, kv_arms = 0, q_arms = 0;
+  if (warp == kProducerWarp || warp == kDOProducerWarp) {
+    // ------------------------------------------------------------ producers
+    // Warp 8: K, V per unit and the Q ring with -lse2; warp 10: the dO ring
+    // with -D. Each stage's row values go in by plain stores from the 32 lanes
+    // before they arrive on the stage's full barrier.
+    const bool q_side = warp == kProducerWarp;
+    const int n_stages = q_side ? L::kQStages : L::kDOStages;
+    const CUtensorMap* tm = q_side ? &tm_q : &tm_do;
+    const uint32_t ring = q_side ? sQ : sDO;
+    float* rowvals = q_side ? lse_s : dsum_s;
+    uint32_t it = 0, kv_arms = 0;
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
@@ -193,70 +228,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int b = bhk / mk.Hkv;
       const int kv_len = kv_len_of(mk, b);
       const int n_kv = (kv_len + kTile - 1) / kTile;
-      if (unit_count > 0 && !mbar_wait_warp(b_kv_empty, (unit_count - 1) & 1, tmo, abort_flag)) {
-        fail();
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        mbar_expect_tx(b_kv_full, 2 * L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_3d(sK + c * 16384, &tm_k, c * 64, kt * kTile, bhk, b_kv_full);
-          tma_load_3d(sV + c * 16384, &tm_v, c * 64, kt * kTile, bhk, b_kv_full);
+      if (q_side) {
+        if (unit_count > 0 &&
+            !mbar_wait_warp(b_kv_empty, (unit_count - 1) & 1, tmo, abort_flag)) {
+          fail();
+          ok = false;
+          break;
         }
+        if (lane == 0) {
+          mbar_expect_tx(b_kv_full, 2 * L::kTileBytes);
+          for (int c = 0; c < L::kChunks; ++c) {
+            tma_load_3d(sK + c * 16384, &tm_k, c * 64, kt * kTile, bhk, b_kv_full);
+            tma_load_3d(sV + c * 16384, &tm_v, c * 64, kt * kTile, bhk, b_kv_full);
+          }
+        }
+        ++kv_arms;
       }
-      ++kv_arms;
       for (int bh = group_first_head<GQA>(mk, bhk), bh_end = bh + G; bh < bh_end && ok;
-             ++bh) {  // the query heads sharing this K/V head
+           ++bh) {  // the query heads sharing this K/V head
         for (int chunk = 0; chunk * 32 < n_t && ok; ++chunk) {
           uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           while (bits != 0u) {
             const int qt = chunk * 32 + (__ffs(bits) - 1);
             bits &= bits - 1;
-            const int s = it % L::kStages;
-            const uint32_t ph = (it / L::kStages) & 1u;
-            if (!mbar_wait_warp(b_q_empty[s], ph ^ 1u, tmo, abort_flag)) {
+            const int s = static_cast<int>(it % static_cast<uint32_t>(n_stages));
+            const uint32_t ph = (it / static_cast<uint32_t>(n_stages)) & 1u;
+            const uint32_t full = q_side ? q_full(s) : do_full(s);
+            if (!mbar_wait_warp(q_side ? q_empty(s) : do_empty(s), ph ^ 1u, tmo, abort_flag)) {
               fail();
               ok = false;
               break;
             }
-            // lse (log2 units) and D of the 128 query rows of this tile
-            float4 l4, d4;
-            float* lp = &l4.x;
-            float* dp = &d4.x;
+            // lse (log2 units) or D of the 128 query rows of this tile, staged
+            // negated: the compute warps add them as packed pairs
+            float4 v4;
+            float* vp = &v4.x;
   #pragma unroll
             for (int r = 0; r < 4; ++r) {
               const int row = qt * kTile + 4 * lane + r;
               const bool in = row < N;
               const long long idx = static_cast<long long>(bh) * N + row;
-              lp[r] = -lse2_of(args.lse, idx, in);
-              dp[r] = in ? -args.dsum[idx] : 0.f;
+              vp[r] = q_side ? -lse2_of(args.lse, idx, in) : (in ? -args.dsum[idx] : 0.f);
             }
-            // staged negated: the compute warps add them as packed pairs
-            reinterpret_cast<float4*>(lse_s + s * 128)[lane] = l4;
-            reinterpret_cast<float4*>(dsum_s + s * 128)[lane] = d4;
+            reinterpret_cast<float4*>(rowvals + s * 128)[lane] = v4;
             if (lane == 0) {
-              mbar_expect_tx(b_q_full[s], 2 * L::kTileBytes);
-              for (int c = 0; c < L::kChunks; ++c) {
-                tma_load_3d(sQ + s * L::kTileBytes + c * 16384, &tm_q, c * 64, qt * kTile, bh,
-                            b_q_full[s]);
-                tma_load_3d(sDO + s * L::kTileBytes + c * 16384, &tm_do, c * 64, qt * kTile, bh,
-                            b_q_full[s]);
-              }
+              mbar_expect_tx(full, L::kTileBytes);
+              for (int c = 0; c < L::kChunks; ++c)
+                tma_load_3d(ring + s * L::kTileBytes + c * 16384, tm, c * 64, qt * kTile, bh, full);
             } else {
-              mbar_arrive(b_q_full[s]);
+              mbar_arrive(full);
             }
-            ++q_arms;
             ++it;
           }
         }
       }
     }
+    // no copy may still be in flight when the block exits
     if (kv_arms) mbar_wait_warp(b_kv_full, (kv_arms - 1) & 1, tmo, nullptr);
-#pragma unroll
-    for (int s = 0; s < L::kStages; ++s)
-      if (q_arms > static_cast<uint32_t>(s))
-        mbar_wait_warp(b_q_full[s], ((q_arms - 1 - s) / L::kStages) & 1, tmo, nullptr);
+    for (int s = 0; s < n_stages; ++s)
+      if (it > static_cast<uint32_t>(s))
+        mbar_wait_warp(q_side ? q_full(s) : do_full(s),
+                       ((it - 1 - s) / static_cast<uint32_t>(n_stages)) & 1, tmo, nullptr);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
@@ -310,16 +342,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t bits = warp_valid_bits_t<WIN>(mk, kt, chunk, n_t, n_kv);
           while (bits != 0u) {
             bits &= bits - 1;
-            const int s = it % L::kStages;
-            const uint32_t ph = (it / L::kStages) & 1u;
-            if (!mbar_wait_warp(b_q_full[s], ph, tmo, abort_flag)) {
+            const int sq = it % L::kQStages, sd = it % L::kDOStages;
+            if (!mbar_wait_warp(q_full(sq), (it / L::kQStages) & 1u, tmo, abort_flag)) {
               fail();
               ok = false;
               break;
             }
             tc_fence_after();
             if (elected) {
-              issue_ss(L::col_st(), sK, sQ + s * L::kTileBytes);  // S^T = K Q^T
+              issue_ss(L::col_st(), sK, sQ + sq * L::kTileBytes);  // S^T = K Q^T
               mma_commit(b_st_full);
             }
             __syncwarp();
@@ -333,12 +364,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               tc_fence_after();
               if (elected) {
                 issue_acc(L::col_dk(), L::col_dpt(), sQ + prev_s * L::kTileBytes, t - 1 > 0);
-                mma_commit(b_q_empty[prev_s]);
+                mma_commit(q_empty(prev_s));
               }
               __syncwarp();
             }
+            if (!mbar_wait_warp(do_full(sd), (it / L::kDOStages) & 1u, tmo, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
             if (elected) {
-              issue_ss(L::col_dpt(), sV, sDO + s * L::kTileBytes);  // dP^T = V dO^T
+              issue_ss(L::col_dpt(), sV, sDO + sd * L::kTileBytes);  // dP^T = V dO^T
               mma_commit(b_dpt_full);
             }
             __syncwarp();
@@ -355,9 +392,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               break;
             }
             tc_fence_after();
-            if (elected) issue_acc(L::col_dv(), L::col_st(), sDO + s * L::kTileBytes, t > 0);
+            if (elected) {
+              issue_acc(L::col_dv(), L::col_st(), sDO + sd * L::kTileBytes, t > 0);
+              mma_commit(do_empty(sd));
+            }
             __syncwarp();
-            prev_s = s;
+            prev_s = sq;
             ++t;
             ++it;
           }
@@ -374,7 +414,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         if (elected) {
           issue_acc(L::col_dk(), L::col_dpt(), sQ + prev_s * L::kTileBytes, t - 1 > 0);
-          mma_commit(b_q_empty[prev_s]);
+          mma_commit(q_empty(prev_s));
         }
         __syncwarp();
       } else if (unit_count > 0) {
@@ -420,9 +460,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           while (bits != 0u) {
             const int qt = chunk * 32 + (__ffs(bits) - 1);
             bits &= bits - 1;
-            const int s = it % L::kStages;
-            const float* lse_t = lse_s + s * 128 + 64 * wg;
-            const float* dsum_t = dsum_s + s * 128 + 64 * wg;
+            const int sq = it % L::kQStages, sd = it % L::kDOStages;
+            const float* lse_t = lse_s + sq * 128 + 64 * wg;
+            const float* dsum_t = dsum_s + sd * 128 + 64 * wg;
             const int q0 = qt * kTile + 64 * wg;  // first query column of this thread's half
             // Dropout keep bits of this (key, 64 queries) strip.
             uint32_t zb0 = 0xFFFFFFFFu, zb1 = 0xFFFFFFFFu;
@@ -549,7 +589,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before();
             mbar_arrive(b_ds_ready);
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_q_empty[s]);  // lse / D of this stage no longer read
+            if (lane == 0) {  // lse and D of these stages no longer read
+              mbar_arrive(q_empty(sq));
+              mbar_arrive(do_empty(sd));
+            }
             ++n_done;
             ++it;
           }
@@ -629,9 +672,10 @@ static cudaError_t launch_dkdv_impl(const CUtensorMap& tq, const CUtensorMap& tk
                          : fa_bwd_dkdv_kernel<D, DROP, true, false>)
                   : (win ? fa_bwd_dkdv_kernel<D, DROP, false, true>
                          : fa_bwd_dkdv_kernel<D, DROP, false, false>);
-  cudaError_t e = set_smem(kern, DkdvLayout<D>::kSmemBytes);
+  constexpr int kSmem = DkdvLayout<D, DROP>::kSmemBytes;
+  cudaError_t e = set_smem(kern, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kBwdThreads, DkdvLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, a);
+  kern<<<grid, kBwdThreads, kSmem, stream>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 

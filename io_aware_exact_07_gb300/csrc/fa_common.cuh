@@ -15,6 +15,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Device status codes (mirror fa_status in include/fa.h).
+constexpr unsigned kStatusCuda = 3u;     // a launch found its configuration unusable
 constexpr unsigned kStatusTimeout = 5u;
 
 struct MaskParams {
