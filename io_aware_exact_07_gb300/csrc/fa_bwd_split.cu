@@ -120,7 +120,7 @@ struct DkdvL {
 };
 
 struct DkdvBars {
-  uint32_t kv_full[2], kv_empty[2], q_full[kMaxQStages], q_empty[kMaxQStages];
+  BarRun kv_full, kv_empty, q_full, q_empty;
   uint32_t st_full, st_free, dpt_full, dpt_free, p_ready, p_done, ds_ready, ds_done;
   uint32_t acc_full, acc_free, drain_a, drain_b;
   uint32_t stall;  // test hook: never completed
@@ -156,10 +156,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   {
     int i = 0;
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
-    for (int b = 0; b < 2; ++b) bars.kv_full[b] = nb();
-    for (int b = 0; b < 2; ++b) bars.kv_empty[b] = nb();
-    for (int s = 0; s < kMaxQStages; ++s) bars.q_full[s] = nb();
-    for (int s = 0; s < kMaxQStages; ++s) bars.q_empty[s] = nb();
+    auto run = [&](int n) {
+      const BarRun r{smem_u32(&bar_mem[i])};
+      i += n;
+      return r;
+    };
+    bars.kv_full = run(2);
+    bars.kv_empty = run(2);
+    bars.q_full = run(kMaxQStages);
+    bars.q_empty = run(kMaxQStages);
     bars.st_full = nb();
     bars.st_free = nb();
     bars.dpt_full = nb();
@@ -683,8 +688,8 @@ struct DqL {
 };
 
 struct DqBars {
-  uint32_t qd_full[2], qd_empty[2], k_full[kMaxKStages], k_empty[kMaxKStages];
-  uint32_t v_full[kMaxVStages], v_empty[kMaxVStages];
+  BarRun qd_full, qd_empty, k_full, k_empty;
+  BarRun v_full, v_empty;
   uint32_t s_full, s_free, dp_full, dp_free, ds_ready, ds_done, dq_full, dq_free;
   uint32_t drain_a, drain_b;
   uint32_t stall;  // test hook: never completed
@@ -726,12 +731,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   {
     int i = 0;
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
-    for (int b = 0; b < 2; ++b) bars.qd_full[b] = nb();
-    for (int b = 0; b < 2; ++b) bars.qd_empty[b] = nb();
-    for (int s = 0; s < kMaxKStages; ++s) bars.k_full[s] = nb();
-    for (int s = 0; s < kMaxKStages; ++s) bars.k_empty[s] = nb();
-    for (int s = 0; s < kMaxVStages; ++s) bars.v_full[s] = nb();
-    for (int s = 0; s < kMaxVStages; ++s) bars.v_empty[s] = nb();
+    auto run = [&](int n) {
+      const BarRun r{smem_u32(&bar_mem[i])};
+      i += n;
+      return r;
+    };
+    bars.qd_full = run(2);
+    bars.qd_empty = run(2);
+    bars.k_full = run(kMaxKStages);
+    bars.k_empty = run(kMaxKStages);
+    bars.v_full = run(kMaxVStages);
+    bars.v_empty = run(kMaxVStages);
     bars.s_full = nb();
     bars.s_free = nb();
     bars.dp_full = nb();

@@ -18,6 +18,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kStatusCuda = 3u;     // a launch found its configuration unusable
 constexpr unsigned kStatusTimeout = 5u;
 
+// A run of consecutive mbarriers (8 bytes each) addressed by index. An array of
+// barrier addresses indexed by a ring stage would be placed in local memory, so
+// every handshake would first load its barrier's address from there.
+struct BarRun {
+  uint32_t base;
+  __device__ __forceinline__ uint32_t operator[](int i) const {
+    return base + 8u * static_cast<uint32_t>(i);
+  }
+};
+
 struct MaskParams {
   int B, H, N;
   int Hkv;                      // K/V heads (H for per-head attention; H / Hkv query heads share one)

@@ -65,9 +65,9 @@ struct DecL {
 
 struct DecBars {
   uint32_t q_full, q_empty;
-  uint32_t k_full[kDecMaxStages], k_empty[kDecMaxStages];
-  uint32_t v_full[kDecMaxStages], v_empty[kDecMaxStages];
-  uint32_t s_full[kSBufs], s_free[kSBufs], p_full[kSBufs];
+  BarRun k_full, k_empty;
+  BarRun v_full, v_empty;
+  BarRun s_full, s_free, p_full;
   uint32_t o_full, o_free, drain, drain_pv, stall;
 };
 
@@ -141,15 +141,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   {
     int i = 0;
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
+    auto run = [&](int n) {
+      const BarRun r{smem_u32(&bar_mem[i])};
+      i += n;
+      return r;
+    };
     bars.q_full = nb();
     bars.q_empty = nb();
-    for (int s = 0; s < kDecMaxStages; ++s) bars.k_full[s] = nb();
-    for (int s = 0; s < kDecMaxStages; ++s) bars.k_empty[s] = nb();
-    for (int s = 0; s < kDecMaxStages; ++s) bars.v_full[s] = nb();
-    for (int s = 0; s < kDecMaxStages; ++s) bars.v_empty[s] = nb();
-    for (uint32_t x = 0; x < kSBufs; ++x) bars.s_full[x] = nb();
-    for (uint32_t x = 0; x < kSBufs; ++x) bars.s_free[x] = nb();
-    for (uint32_t x = 0; x < kSBufs; ++x) bars.p_full[x] = nb();
+    bars.k_full = run(kDecMaxStages);
+    bars.k_empty = run(kDecMaxStages);
+    bars.v_full = run(kDecMaxStages);
+    bars.v_empty = run(kDecMaxStages);
+    bars.s_full = run(kSBufs);
+    bars.s_free = run(kSBufs);
+    bars.p_full = run(kSBufs);
     bars.o_full = nb();
     bars.o_free = nb();
     bars.drain = nb();

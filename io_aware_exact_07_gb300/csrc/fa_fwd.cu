@@ -83,10 +83,11 @@ struct FwdLayout {
 };
 
 struct Bars {
-  uint32_t q_full[2], q_empty;
-  uint32_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint32_t s_full[2], p_full[2], o_full[2], o_free[2];
-  uint32_t s_free[2], pv_done[2];  // decoupled schedule only
+  BarRun q_full;
+  uint32_t q_empty;
+  BarRun k_full, k_empty, v_full, v_empty;
+  BarRun s_full, p_full, o_full, o_free;
+  BarRun s_free, pv_done;  // decoupled schedule only
   uint32_t drain, drain2, stall;
 };
 
@@ -143,19 +144,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   {
     int i = 0;
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
-    bars.q_full[0] = nb();
-    bars.q_full[1] = nb();
+    auto run = [&](int n) {
+      const BarRun r{smem_u32(&bar_mem[i])};
+      i += n;
+      return r;
+    };
+    bars.q_full = run(2);
     bars.q_empty = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.k_full[s] = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.k_empty[s] = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.v_full[s] = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.v_empty[s] = nb();
-    for (int x = 0; x < 2; ++x) bars.s_full[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.p_full[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.o_full[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.o_free[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.s_free[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.pv_done[x] = nb();
+    bars.k_full = run(L::kStages);
+    bars.k_empty = run(L::kStages);
+    bars.v_full = run(L::kStages);
+    bars.v_empty = run(L::kStages);
+    bars.s_full = run(2);
+    bars.p_full = run(2);
+    bars.o_full = run(2);
+    bars.o_free = run(2);
+    bars.s_free = run(2);
+    bars.pv_done = run(2);
     bars.drain = nb();
     bars.drain2 = nb();
     bars.stall = nb();

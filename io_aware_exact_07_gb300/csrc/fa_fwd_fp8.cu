@@ -62,10 +62,10 @@ struct F8L {
 };
 
 struct F8Bars {
-  uint32_t q_full[2], q_empty;
-  uint32_t k_full[F8L::kStages], k_empty[F8L::kStages], v_full[F8L::kStages],
-      v_empty[F8L::kStages];
-  uint32_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
+  BarRun q_full;
+  uint32_t q_empty;
+  BarRun k_full, k_empty, v_full, v_empty;
+  BarRun s_full, s_free, p_full, pv_done, o_free;
   uint32_t drain, drain2, stall;
 };
 
@@ -122,18 +122,22 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   {
     int i = 0;
     auto nb = [&]() { return smem_u32(&bar_mem[i++]); };
-    bars.q_full[0] = nb();
-    bars.q_full[1] = nb();
+    auto run = [&](int n) {
+      const BarRun r{smem_u32(&bar_mem[i])};
+      i += n;
+      return r;
+    };
+    bars.q_full = run(2);
     bars.q_empty = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.k_full[s] = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.k_empty[s] = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.v_full[s] = nb();
-    for (int s = 0; s < L::kStages; ++s) bars.v_empty[s] = nb();
-    for (int x = 0; x < 2; ++x) bars.s_full[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.s_free[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.p_full[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.pv_done[x] = nb();
-    for (int x = 0; x < 2; ++x) bars.o_free[x] = nb();
+    bars.k_full = run(L::kStages);
+    bars.k_empty = run(L::kStages);
+    bars.v_full = run(L::kStages);
+    bars.v_empty = run(L::kStages);
+    bars.s_full = run(2);
+    bars.s_free = run(2);
+    bars.p_full = run(2);
+    bars.pv_done = run(2);
+    bars.o_free = run(2);
     bars.drain = nb();
     bars.drain2 = nb();
     bars.stall = nb();
