@@ -52,7 +52,7 @@ struct TileT {
 };
 
 // Barrier arrays are sized for the deepest ring of either head size.
-constexpr int kMaxQStages = 3;  // dK/dV kernel: Q / dO ring
+constexpr int kMaxQStages = 4;  // dK/dV kernel: Q / dO ring
 constexpr int kMaxKStages = 4;  // dQ kernel: K ring
 constexpr int kMaxVStages = 3;  // dQ kernel: V ring
 
@@ -101,7 +101,7 @@ struct DkdvL {
   static constexpr int T = TileT<D>::kBytes;
   static constexpr bool kSepBuf = (D == 64);       // separate P^T / dS^T buffers
   static constexpr int kKVBufs = (D == 64) ? 2 : 1;
-  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
   static_assert(kStages <= kMaxQStages, "Q / dO ring deeper than its barrier arrays");
   static constexpr int kKVOff = 0;                                   // kKVBufs x (K, V)
   static constexpr int kQOff = kKVBufs * 2 * T;
