@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_t = (N + kTile - 1) / kTile;
   const int n_units = mk.B * mk.Hkv * n_t;
   const int G = GQA ? mk.H / mk.Hkv : 1;  // query heads per K/V head
+  const bool rot = mk.seqlens_k != nullptr;  // rotated schedule under key padding
 
   uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, q_arms = 0, kv_arms[2] = {0, 0};
       bool ok = true;
       int unit_count = 0;
-      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+      for (int u = sched_unit(0, rot); u < n_units && ok; u = sched_unit(++unit_count, rot)) {
         const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
         const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
         const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       int unit_count = 0;
-      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+      for (int u = sched_unit(0, rot); u < n_units && ok; u = sched_unit(++unit_count, rot)) {
         const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
         const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
         const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, prc = 0, dsc = 0;
       bool ok = true;
       int unit_count = 0;
-      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+      for (int u = sched_unit(0, rot); u < n_units && ok; u = sched_unit(++unit_count, rot)) {
         const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
         const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
         const int n_kv = (kv_len + kTile - 1) / kTile;
@@ -446,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, gt = 0, stc = 0, dpc = 0, pdc = 0, dsc = 0;
     bool ok = true;
     int unit_count = 0;
-    for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+    for (int u = sched_unit(0, rot); u < n_units && ok; u = sched_unit(++unit_count, rot)) {
       const int bhk = u / n_t, kt = u % n_t;  // K/V head, key tile
       const int kv_len = kv_len_of(mk, bhk / mk.Hkv);
       const int n_kv = (kv_len + kTile - 1) / kTile;

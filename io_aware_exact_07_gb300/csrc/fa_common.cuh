@@ -90,8 +90,14 @@ __device__ __forceinline__ int kv_len_of(const MaskParams& m, int b) {
 // each other; head-major order keeps the CTAs of a round on a few heads, whose
 // K/V tiles they then share in L2. Returns a position >= the list length once
 // the CTA has no more work (positions grow with k).
-__device__ __forceinline__ int sched_unit(int k) {
+// With rotate set, round k instead shifts the positions by k: the dK/dV work
+// list under key padding has its empty units (key tiles past a batch row's
+// length) at the same places in every head, so the alternation would hand some
+// CTAs a key tile and its mirror, both often empty, in every round, and others
+// none; rotating lets every CTA meet every key tile.
+__device__ __forceinline__ int sched_unit(int k, bool rotate = false) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  if (rotate) return k * G + (c + k) % G;
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
