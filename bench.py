@@ -103,7 +103,7 @@ def load_peaks():
 # Sources each timed kernel is built from: a committed DRAM-traffic figure is
 # used only while these files are unchanged since it was captured.
 KERNEL_SOURCES = {
-    "fwd": ("fa_fwd.cu", "fa_kernels.h"),
+    "fwd": ("fa_fwd.cu", "fa_fwd128.cu", "fa_kernels.h"),
     "bwd_dkdv": ("fa_bwd.cu", "fa_bwd_split.cu", "fa_kernels.h"),
     "bwd_dq": ("fa_bwd_split.cu", "fa_kernels.h"),
     "bwd_preprocess": ("fa_bwd.cu", "fa_kernels.h"),

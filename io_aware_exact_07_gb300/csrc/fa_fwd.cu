@@ -1,25 +1,27 @@
-// Forward pass of exact attention on sm_103a: tiled S = Q K^T, online softmax
-// with a running maximum m and sum l, O += P V, writing only O and the row
-// logsumexp (FlashAttention deep-read report, sections 2.4 and 3.2; Attention
-// Kernel page, "FlashAttention's insight: IO-aware").
+// Forward pass of exact attention at head dimension 64 on sm_103a: tiled
+// S = Q K^T, online softmax with a running maximum m and sum l, O += P V,
+// writing only O and the row logsumexp (FlashAttention deep-read report,
+// sections 2.4 and 3.2; Attention Kernel page, "FlashAttention's insight:
+// IO-aware"). Head dimension 128 has its own kernel (fa_fwd128.cu).
 //
 // Design (per CTA, persistent over work units; one unit = one (b, h) head and
 // a block of 256 query rows split into two 128-row query tiles "a" and "b"):
 //   warp 8      TMA producer: Q_a, Q_b once per unit, then K_j / V_j tiles
-//               through an NS-stage shared-memory ring (128-byte swizzle).
-//   warp 9      MMA issuer (one elected lane): S_x = Q_x K_j^T with
-//               tcgen05.mma (both operands in shared memory, fp32 accumulator
-//               in tensor memory) and O_x += P_x V_j with P_x read from
-//               tensor memory (bf16) and V_j from shared memory.
+//               through a four-stage shared-memory ring (128-byte swizzle).
+//   warp 9      S issuer (one elected lane): S_x = Q_x K_j^T with tcgen05.mma
+//               (both operands in shared memory, fp32 accumulator in tensor
+//               memory) as soon as the softmax has read the previous S_x.
+//   warp 10     PV issuer (one elected lane): O_x += P_x V_j with P_x read
+//               from tensor memory (bf16) and V_j from shared memory.
 //   warps 0-3   softmax + correction for query tile a (thread = query row,
 //   warps 4-7   ... and tile b): tcgen05.ld of the S row, masking, row max,
-//               exp2-based probabilities, running sum, dropout, P written back
-//               to tensor memory over S as bf16, in-place rescale of the O row
-//               when the running maximum grows by more than 2^8; the epilogue
-//               divides by l and writes O (bf16) and lse (fp32).
+//               exp2-based probabilities, running sum, dropout, P written to
+//               its own tensor-memory buffer as bf16, in-place rescale of the O
+//               row when the running maximum grows by more than 2^8; the
+//               epilogue divides by l and writes O (bf16) and lse (fp32).
 // The two query tiles ping-pong: while the softmax warps of one tile work,
-// the tensor core runs the other tile's GEMMs. Tensor memory holds
-// S_a, S_b (128 columns each) and O_a, O_b (d columns each).
+// the tensor core runs the other tile's GEMMs. Tensor memory holds S_a, S_b
+// (128 columns each), P_a, P_b and O_a, O_b (64 columns each).
 //
 // Loop order differs from the pages' Algorithm 1 (K/V outer, Q inner, O and
 // (m, l) written back every step): here the query tile is outer and stays on
@@ -38,7 +40,7 @@ namespace {
 constexpr int kSoftmaxWarps = 8;  // two warpgroups, one per query tile
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kPvWarp = 10;  // second MMA issuer (decoupled schedule)
+constexpr int kPvWarp = 10;  // second MMA issuer
 // Warp 11 idles: it completes the third warpgroup, since registers move between
 // whole warpgroups.
 constexpr int kFwdThreads = 12 * 32;
@@ -55,39 +57,33 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when m grows
 
 template <int D>
 struct FwdLayout {
+  static_assert(D == 64, "head dimension 128 runs the kernel of fa_fwd128.cu");
   static constexpr int kChunks = D / 64;                 // 64-column (128-byte) swizzle chunks
   static constexpr int kTileBytes = kTile * D * 2;       // one 128 x D bf16 tile
-  static constexpr int kStages = (D == 64) ? 4 : 2;      // K/V ring depth
-  static_assert(kStages <= 4, "the K/V ring's barrier arrays hold four stages");
+  static constexpr int kStages = 4;                      // K/V ring depth
   static constexpr int kQOff = 0;                        // Q_a, Q_b
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // barriers: q_full[2], q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S],
-  //           s_full[2], p_full[2], o_full[2], o_free[2], s_free[2], pv_done[2], drain, stall
-  static constexpr int kNumBars = 2 + 1 + 4 * kStages + 12 + 3;
+  //           s_full[2], p_full[2], o_free[2], s_free[2], pv_done[2], drain, drain2, stall
+  static constexpr int kNumBars = 2 + 1 + 4 * kStages + 10 + 3;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + slack for 1024-byte alignment
-  // At d = 64 tensor memory has room for a separate P buffer per query tile
+  // Tensor memory has room for a separate P buffer per query tile
   // (2 x (128 S + 64 P + 64 O) = 512 columns), so the next S can be computed
-  // while the softmax still works on the current one. At d = 128 P is written
-  // over S (2 x (128 S + 128 O) = 512 columns).
-  static constexpr bool kSepP = (D == 64);
+  // while the softmax still works on the current one.
   __device__ static constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
-  __device__ static constexpr uint32_t col_p(int x) {
-    return kSepP ? 256u + 64u * static_cast<uint32_t>(x) : col_s(x);
-  }
-  __device__ static constexpr uint32_t col_o(int x) {
-    return kSepP ? 384u + 64u * static_cast<uint32_t>(x) : 256u + static_cast<uint32_t>(x * D);
-  }
+  __device__ static constexpr uint32_t col_p(int x) { return 256u + 64u * static_cast<uint32_t>(x); }
+  __device__ static constexpr uint32_t col_o(int x) { return 384u + 64u * static_cast<uint32_t>(x); }
 };
 
 struct Bars {
   BarRun q_full;
   uint32_t q_empty;
   BarRun k_full, k_empty, v_full, v_empty;
-  BarRun s_full, p_full, o_full, o_free;
-  BarRun s_free, pv_done;  // decoupled schedule only
+  BarRun s_full, p_full, o_free;
+  BarRun s_free, pv_done;
   uint32_t drain, drain2, stall;
 };
 
@@ -118,10 +114,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
   using L = FwdLayout<D>;
-  // P in its own buffer (d = 64): without dropout each half of P is stored as
-  // soon as it is formed; with dropout (more live registers) both halves are
-  // stored at the end, which keeps that instance free of spills.
-  constexpr bool kEarlyP = L::kSepP && !DROPOUT;
+  // Without dropout each half of P is stored as soon as it is formed; with
+  // dropout (more live registers) both halves are stored at the end, which keeps
+  // that instance free of spills.
+  constexpr bool kEarlyP = !DROPOUT;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -157,7 +153,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bars.v_empty = run(L::kStages);
     bars.s_full = run(2);
     bars.p_full = run(2);
-    bars.o_full = run(2);
     bars.o_free = run(2);
     bars.s_free = run(2);
     bars.pv_done = run(2);
@@ -180,8 +175,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(bars.s_full[x], 1);
       mbar_init(bars.p_full[x], 128);
-      mbar_init(bars.o_full[x], 1);
-      mbar_init(bars.o_free[x], 128);
+      // o_free[x]: the 128 softmax threads of tile x at the end of each
+      // epilogue, plus the PV issuer once per unit after its own wait on the
+      // previous phase, so that no phase can complete while the PV issuer still
+      // waits on the one before it (units without key tiles would otherwise let
+      // the epilogues run ahead).
+      mbar_init(bars.o_free[x], 129);
       mbar_init(bars.s_free[x], 128);
       mbar_init(bars.pv_done[x], 1);
     }
@@ -298,21 +297,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_wait_warp(bars.q_full[1], (q_armed - 1) & 1, tmo, nullptr);
       }
     } else if (warp == kMmaWarp) {
-      // ------------------------------------------------------------ MMA issuer
+      // ------------------------------------------------------------ S issuer
       // Lane 0 alone waits and issues: tcgen05.mma issue blocks while the tensor
       // core is busy (its queue is shallow), so every cycle this thread spends on
       // anything else is a tensor-core bubble. The rest of the warp only helps
       // evaluate the tile lists (one ballot per 32 key tiles).
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
-      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);   // O += P V, V MN-major
       constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
       const bool leader = (lane == 0);
       const uint64_t dQa = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dQb = sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
       const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
       uint32_t it = 0;
-      uint32_t p_cnt0 = 0, p_cnt1 = 0, sf_cnt0 = 0, sf_cnt1 = 0;
+      uint32_t sf_cnt0 = 0, sf_cnt1 = 0;
       bool s_seen0 = false, s_seen1 = false;
       bool ok = true;
       if (args.sync.inject_stall && leader) {
@@ -333,14 +330,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         mma_commit(bars.s_full[x]);
       };
-      auto issue_PV = [&](int x, int s, bool first) {
-        const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
-  #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
-                 dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
-                 (first && kk == 0) ? 0u : 1u);
-      };
       int unit_count = 0;
       for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
         const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
@@ -349,24 +338,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int jmax = n_kv;
         if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
         const uint32_t uph = unit_count & 1;
-        bool pend0 = false, pend1 = false, first0 = true, first1 = true;
-        int prev_stage = -1;
-        uint32_t prev_ph = 0;
-        // PV of query tile x for the tile S-issued at the previous ring position.
-        auto pv = [&](int x) -> bool {
-          uint32_t& pc = x ? p_cnt1 : p_cnt0;
-          bool& first = x ? first1 : first0;
-          if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
-          ++pc;
-          if (first && unit_count > 0 &&
-              !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
-            return false;
-          tc_fence_after();
-          issue_PV(x, prev_stage, first);
-          if constexpr (L::kSepP) mma_commit(bars.pv_done[x]);
-          first = false;
-          return true;
-        };
         if (leader) {
           ok = mbar_wait(bars.q_full[0], uph, tmo, abort_flag) &&
                mbar_wait(bars.q_full[1], uph, tmo, abort_flag);
@@ -388,84 +359,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 ok = false;
                 break;
               }
-              if constexpr (L::kSepP) {
-                // S of this position as soon as the softmax has read the previous S ...
-                if (v0) {
-                  if (s_seen0 && !mbar_wait(bars.s_free[0], sf_cnt0++ & 1, tmo, abort_flag)) {
-                    ok = false;
-                    break;
-                  }
-                  tc_fence_after();
-                  issue_S(0, s);
-                  s_seen0 = true;
-                }
-                if (v1) {
-                  if (s_seen1 && !mbar_wait(bars.s_free[1], sf_cnt1++ & 1, tmo, abort_flag)) {
-                    ok = false;
-                    break;
-                  }
-                  tc_fence_after();
-                  issue_S(1, s);
-                  s_seen1 = true;
-                }
-                // (the PVs come from the PV-issuer warp)
-              } else {
-                // P is written over S: PV of the previous tile of x must be issued
-                // before the next S of x.
-                if (prev_stage >= 0 &&
-                    !mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag)) {
+              // S of this position as soon as the softmax has read the previous S
+              // (the PVs come from the PV-issuer warp)
+              if (v0) {
+                if (s_seen0 && !mbar_wait(bars.s_free[0], sf_cnt0++ & 1, tmo, abort_flag)) {
                   ok = false;
                   break;
                 }
-                const bool had_pv = pend0 || pend1;
-                if (pend0 && !pv(0)) {
+                tc_fence_after();
+                issue_S(0, s);
+                s_seen0 = true;
+              }
+              if (v1) {
+                if (s_seen1 && !mbar_wait(bars.s_free[1], sf_cnt1++ & 1, tmo, abort_flag)) {
                   ok = false;
                   break;
                 }
-                if (v0) issue_S(0, s);
-                if (pend1 && !pv(1)) {
-                  ok = false;
-                  break;
-                }
-                if (v1) issue_S(1, s);
-                if (had_pv) mma_commit(bars.v_empty[prev_stage]);
+                tc_fence_after();
+                issue_S(1, s);
+                s_seen1 = true;
               }
               mma_commit(bars.k_empty[s]);
-              pend0 = v0;
-              pend1 = v1;
-              prev_stage = s;
-              prev_ph = ph;
               ++it;
             }
             if (!ok) fail();
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        if (leader && ok && L::kSepP) {
-          mma_commit(bars.q_empty);
-        } else if (leader && ok) {
-          // Flush the PVs of the last position, then release it.
-          if (prev_stage >= 0) {
-            ok = mbar_wait(bars.v_full[prev_stage], prev_ph, tmo, abort_flag) &&
-                 (!pend0 || pv(0)) && (!pend1 || pv(1));
-            if (ok) mma_commit(bars.v_empty[prev_stage]);
-          }
-          // A query tile without PV in this unit still consumes the epilogue
-          // handshake of the previous unit.
-          if (ok && first0 && unit_count > 0)
-            ok = mbar_wait(bars.o_free[0], (unit_count - 1) & 1, tmo, abort_flag);
-          if (ok && first1 && unit_count > 0)
-            ok = mbar_wait(bars.o_free[1], (unit_count - 1) & 1, tmo, abort_flag);
-          if (ok) {
-            if constexpr (!L::kSepP) {
-              mma_commit(bars.o_full[0]);
-              mma_commit(bars.o_full[1]);
-            }
-            mma_commit(bars.q_empty);
-          } else {
-            fail();
-          }
-        }
+        // Q is free for the next unit once the last S of this one has completed.
+        if (leader && ok) mma_commit(bars.q_empty);
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       // Drain: all issued MMAs must finish before tensor memory is released.
@@ -476,83 +398,88 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __syncwarp();
     } else if (warp == kPvWarp) {
       // ------------------------------------------------------------ PV issuer
-      // Decoupled schedule only: O_x += P_x V_j as soon as P_x of key tile j is
-      // ready, from a second issuing thread, so that the tensor core keeps
-      // receiving work while the S issuer waits on its own barriers. Its MMAs are
-      // tracked by its own commits (pv_done, v_empty).
-      if constexpr (L::kSepP) {
-        constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);
-        constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
-        const bool leader = (lane == 0);
-        const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
-        uint32_t it = 0, p_cnt0 = 0, p_cnt1 = 0;
-        bool ok = true;
-        int unit_count = 0;
-        for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
-          const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
-          const int kv_len = kv_len_of(mk, uc.b);
-          const int n_kv = (kv_len + kTile - 1) / kTile;
-          int jmax = n_kv;
-          if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
-          bool first0 = true, first1 = true;
-          auto pv = [&](int x, int s) -> bool {
-            uint32_t& pc = x ? p_cnt1 : p_cnt0;
-            bool& first = x ? first1 : first0;
-            if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
-            ++pc;
-            if (first && unit_count > 0 &&
-                !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
-              return false;
-            tc_fence_after();
-            const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
+      // O_x += P_x V_j as soon as P_x of key tile j is ready, from a second
+      // issuing thread, so that the tensor core keeps receiving work while the S
+      // issuer waits on its own barriers. Its MMAs are tracked by its own commits
+      // (pv_done, v_empty).
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);  // O += P V, V MN-major
+      constexpr uint64_t kStageStep = static_cast<uint64_t>(L::kTileBytes >> 4);
+      const bool leader = (lane == 0);
+      const uint64_t dV0 = sdesc_sw128(sV, 16384, 1024);
+      uint32_t it = 0, p_cnt0 = 0, p_cnt1 = 0;
+      bool ok = true;
+      int unit_count = 0;
+      for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
+        const UnitCoord uc = decode_unit(u, BH, mk.H, n_qblk, mk.causal);
+        const int kv_len = kv_len_of(mk, uc.b);
+        const int n_kv = (kv_len + kTile - 1) / kTile;
+        int jmax = n_kv;
+        if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
+        bool first0 = true, first1 = true;
+        // The first PV of query tile x in a unit overwrites O_x, which the
+        // previous unit's epilogue reads: it waits for that epilogue (o_free[x])
+        // and adds this issuer's arrival for the current unit.
+        auto claim_o = [&](int x) -> bool {
+          if (unit_count > 0 && !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
+            return false;
+          mbar_arrive(bars.o_free[x]);
+          return true;
+        };
+        auto pv = [&](int x, int s, bool first) -> bool {
+          // (counters selected by value: a reference to either would put both in
+          // local memory)
+          const uint32_t pc = x ? p_cnt1 : p_cnt0;
+          if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
+          if (x) ++p_cnt1; else ++p_cnt0;
+          if (first && !claim_o(x)) return false;
+          tc_fence_after();
+          const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStageStep;
   #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
-                     dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
-                     (first && kk == 0) ? 0u : 1u);
-            mma_commit(bars.pv_done[x]);
-            first = false;
-            return true;
-          };
-          for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
-            const uint32_t va = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv);
-            const uint32_t vb = warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
-            if (leader) {
-              uint32_t bits = va | vb;
-              while (bits != 0u && ok) {
-                const int bit = __ffs(bits) - 1;
-                bits &= bits - 1;
-                const int s = it % L::kStages;
-                const uint32_t ph = (it / L::kStages) & 1u;
-                if (!mbar_wait(bars.v_full[s], ph, tmo, abort_flag) ||
-                    (((va >> bit) & 1u) && !pv(0, s)) || (((vb >> bit) & 1u) && !pv(1, s))) {
-                  ok = false;
-                  break;
-                }
-                mma_commit(bars.v_empty[s]);
-                ++it;
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + L::col_o(x), tmem + L::col_p(x) + kk * 8,
+                   dv + static_cast<uint64_t>((kk * 2048) >> 4), kIdPV,
+                   (first && kk == 0) ? 0u : 1u);
+          mma_commit(bars.pv_done[x]);
+          return true;
+        };
+        for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
+          const uint32_t va = warp_valid_bits<WIN>(mk, uc.qt0, chunk, n_q, n_kv);
+          const uint32_t vb = warp_valid_bits<WIN>(mk, uc.qt0 + 1, chunk, n_q, n_kv);
+          if (leader) {
+            uint32_t bits = va | vb;
+            while (bits != 0u && ok) {
+              const int bit = __ffs(bits) - 1;
+              bits &= bits - 1;
+              const bool v0 = ((va >> bit) & 1u) != 0u, v1 = ((vb >> bit) & 1u) != 0u;
+              const int s = it % L::kStages;
+              const uint32_t ph = (it / L::kStages) & 1u;
+              if (!mbar_wait(bars.v_full[s], ph, tmo, abort_flag) || (v0 && !pv(0, s, first0)) ||
+                  (v1 && !pv(1, s, first1))) {
+                ok = false;
+                break;
               }
-              if (!ok) fail();
+              if (v0) first0 = false;
+              if (v1) first1 = false;
+              mma_commit(bars.v_empty[s]);
+              ++it;
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-          }
-          if (leader && ok) {
-            // A query tile without PV in this unit still consumes the epilogue
-            // handshake of the previous unit.
-            if (first0 && unit_count > 0)
-              ok = mbar_wait(bars.o_free[0], (unit_count - 1) & 1, tmo, abort_flag);
-            if (ok && first1 && unit_count > 0)
-              ok = mbar_wait(bars.o_free[1], (unit_count - 1) & 1, tmo, abort_flag);
             if (!ok) fail();
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        if (leader) {
-          mma_commit(bars.drain2);
-          mbar_wait(bars.drain2, 0, tmo, nullptr);
+        if (leader && ok) {
+          // A query tile without PV in this unit still consumes the epilogue
+          // handshake of the previous unit and adds its arrival.
+          ok = (!first0 || claim_o(0)) && (!first1 || claim_o(1));
+          if (!ok) fail();
         }
-        __syncwarp();
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
+      if (leader) {
+        mma_commit(bars.drain2);
+        mbar_wait(bars.drain2, 0, tmo, nullptr);
+      }
+      __syncwarp();
     }
   } else {
     regs_inc<kRegsSoftmax>();
@@ -566,7 +493,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + lane_base + L::col_o(x);
     const float c_log2 = args.scale_log2;
     uint32_t s_cnt = 0;
-    uint32_t pv_cnt = 0;  // decoupled schedule: PV completions consumed
+    uint32_t pv_cnt = 0;  // PV completions consumed
     bool ok = true;
     int unit_count = 0;
     for (int u = sched_unit(0); u < n_units && ok; u = sched_unit(++unit_count)) {
@@ -605,11 +532,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, &sr[c * 32]);
           tmem_ld_wait();
-          if constexpr (L::kSepP) {
-            // S is in registers: the next S may be written over it.
-            tc_fence_before();
-            mbar_arrive(bars.s_free[x]);
-          }
+          // S is in registers: the next S may be written over it.
+          tc_fence_before();
+          mbar_arrive(bars.s_free[x]);
           float s[128];
 #pragma unroll
           for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(sr[k]);
@@ -698,11 +623,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 tc_fence_after();
               }
               tmem_st32(tP + half * 32, &pk[half * 32]);
-            } else if constexpr (!L::kSepP) {
-              tmem_st32(tS + half * 32, &pk[half * 32]);
             }
           }
-          if constexpr (L::kSepP && !kEarlyP) {
+          if constexpr (!kEarlyP) {
             // The previous PV reads the P buffer and accumulates into O: wait for it.
             if (n_done > 0) {
               if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
@@ -736,7 +659,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               tmem_st32(tO + c * 32, o);
             }
           }
-          if constexpr (L::kSepP && !kEarlyP) {
+          if constexpr (!kEarlyP) {
             tmem_st32(tP, &pk[0]);
             tmem_st32(tP + 32, &pk[32]);
           }
@@ -748,22 +671,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: O = acc * keep_scale / l, lse = (m + log2 l) * ln 2
-      if constexpr (L::kSepP) {
-        // the last PV of this unit has completed once its pv_done phase has
-        if (n_done > 0) {
-          if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          ++pv_cnt;
-        }
-      } else {
-        if (!mbar_wait_warp(bars.o_full[x], unit_count & 1, tmo, abort_flag)) {
+      // the last PV of this unit has completed once its pv_done phase has
+      if (n_done > 0) {
+        if (!mbar_wait_warp(bars.pv_done[x], pv_cnt & 1, tmo, abort_flag)) {
           fail();
           ok = false;
           break;
         }
+        ++pv_cnt;
       }
       tc_fence_after();
       const bool row_ok = row < N;
@@ -831,16 +746,13 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, int d, bool dropout, int num_sms, cudaStream_t stream) {
+  if (d == 128) return launch_fwd128(tq, tk, tv, a, dropout, num_sms, stream);
   const int n_q = (a.mask.N + kTile - 1) / kTile;
   const long long units = static_cast<long long>(a.mask.B) * a.mask.H * ((n_q + 1) / 2);
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   if (grid <= 0) return cudaSuccess;
-  if (d == 64) {
-    return dropout ? launch_fwd_impl<64, true>(tq, tk, tv, a, grid, stream)
-                   : launch_fwd_impl<64, false>(tq, tk, tv, a, grid, stream);
-  }
-  return dropout ? launch_fwd_impl<128, true>(tq, tk, tv, a, grid, stream)
-                 : launch_fwd_impl<128, false>(tq, tk, tv, a, grid, stream);
+  return dropout ? launch_fwd_impl<64, true>(tq, tk, tv, a, grid, stream)
+                 : launch_fwd_impl<64, false>(tq, tk, tv, a, grid, stream);
 }
 
 }  // namespace fa

@@ -158,7 +158,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       mbar_init(bars.s_free[x], 128);
       mbar_init(bars.p_full[x], 128);
       mbar_init(bars.pv_done[x], 1);
-      mbar_init(bars.o_free[x], 128);
+      // o_free[x]: the 128 softmax threads of tile x at the end of each
+      // epilogue, plus the PV issuer once per unit after its own wait on the
+      // previous phase, so that no phase can complete while the PV issuer still
+      // waits on the one before it.
+      mbar_init(bars.o_free[x], 129);
     }
     mbar_init(bars.drain, 1);
     mbar_init(bars.drain2, 1);
@@ -362,14 +366,22 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       int jmax = n_kv;
       if (mk.causal && uc.qt0 + 2 < jmax) jmax = uc.qt0 + 2;
       bool first0 = true, first1 = true;
-      auto pv = [&](int x, int s) -> bool {
-        uint32_t& pc = x ? p_cnt1 : p_cnt0;
-        bool& first = x ? first1 : first0;
-        if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
-        ++pc;
-        if (first && unit_count > 0 &&
-            !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
+      // The first PV of query tile x in a unit overwrites O_x, which the previous
+      // unit's epilogue reads: it waits for that epilogue (o_free[x]) and adds
+      // this issuer's arrival for the current unit.
+      auto claim_o = [&](int x) -> bool {
+        if (unit_count > 0 && !mbar_wait(bars.o_free[x], (unit_count - 1) & 1, tmo, abort_flag))
           return false;
+        mbar_arrive(bars.o_free[x]);
+        return true;
+      };
+      auto pv = [&](int x, int s, bool first) -> bool {
+        // (counters selected by value: a reference to either would put both in
+        // local memory)
+        const uint32_t pc = x ? p_cnt1 : p_cnt0;
+        if (!mbar_wait(bars.p_full[x], pc & 1, tmo, abort_flag)) return false;
+        if (x) ++p_cnt1; else ++p_cnt0;
+        if (first && !claim_o(x)) return false;
         tc_fence_after();
         const uint64_t dp = x ? dPb : dPa;
         const uint64_t dv = dV0 + static_cast<uint64_t>(s) * kStep;
@@ -379,7 +391,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           mma_ss_f8(tmem + L::col_o(x), dp + off, dv + off, kId, (first && kk == 0) ? 0u : 1u);
         }
         mma_commit(bars.pv_done[x]);
-        first = false;
         return true;
       };
       for (int chunk = 0; chunk * 32 < jmax && ok; ++chunk) {
@@ -390,12 +401,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           while (bits != 0u && ok) {
             const int bit = __ffs(bits) - 1;
             bits &= bits - 1;
+            const bool v0 = ((va >> bit) & 1u) != 0u, v1 = ((vb >> bit) & 1u) != 0u;
             const int s = it % L::kStages;
             if (!mbar_wait(bars.v_full[s], (it / L::kStages) & 1u, tmo, abort_flag) ||
-                (((va >> bit) & 1u) && !pv(0, s)) || (((vb >> bit) & 1u) && !pv(1, s))) {
+                (v0 && !pv(0, s, first0)) || (v1 && !pv(1, s, first1))) {
               ok = false;
               break;
             }
+            if (v0) first0 = false;
+            if (v1) first1 = false;
             mma_commit(bars.v_empty[s]);
             ++it;
           }
@@ -404,11 +418,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (leader && ok) {
-        // a query tile without keys in this unit still consumes the epilogue handshake
-        if (first0 && unit_count > 0)
-          ok = mbar_wait(bars.o_free[0], (unit_count - 1) & 1, tmo, abort_flag);
-        if (ok && first1 && unit_count > 0)
-          ok = mbar_wait(bars.o_free[1], (unit_count - 1) & 1, tmo, abort_flag);
+        // a query tile without keys in this unit still consumes the epilogue
+        // handshake and adds its arrival
+        ok = (!first0 || claim_o(0)) && (!first1 || claim_o(1));
         if (!ok) fail();
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);

@@ -37,6 +37,10 @@ struct BwdArgs {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, int d, bool dropout, int num_sms, cudaStream_t stream);
 
+// d = 128 forward (fa_fwd128.cu); launch_fwd routes d = 128 there.
+cudaError_t launch_fwd128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const FwdArgs& a, bool dropout, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, int d, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -147,6 +147,28 @@ def test_fp8_end_to_end_rotation_helps_with_outliers():
     assert errs[True][0] < errs[False][0] and errs[True][1] < errs[False][1], errs
 
 
+def test_fp8_long_runs_of_empty_units():
+    """Key lengths 0 for all batch rows but the last, with several work units per
+    CTA: the empty rows give O = 0 and lse = -inf, and the last row equals the
+    same kernel run on it alone, bit for bit."""
+    B, H, N, d = 16, 16, 1024, 128
+    x = inputs.draw_fp8_codes(B, H, N, d, seed=5)
+    Np = fa.fa_fp8_vt_stride(N)
+    vt = torch.zeros((B, H, d, Np), dtype=torch.uint8)
+    vt[..., :N] = x["v8"].transpose(2, 3)
+    sl = torch.zeros(B, dtype=torch.int32)
+    sl[-1] = N - 5
+    z = dict(q8=x["q8"].cuda(), k8=x["k8"].cuda(), vt8=vt.contiguous().cuda(),
+             s_q=x["s_q"].cuda(), s_k=x["s_k"].cuda(), s_v=x["s_v"].cuda())
+    z1 = {n: t[-1:].contiguous() for n, t in z.items()}
+    o, lse = fa.fwd_fp8(z, 0.088, seqlens_k=sl.cuda())
+    o1, lse1 = fa.fwd_fp8(z1, 0.088, seqlens_k=sl[-1:].cuda())
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    assert torch.all(o[:-1] == 0) and torch.all(torch.isneginf(lse[:-1]))
+    assert torch.equal(o[-1:], o1) and torch.equal(lse[-1:], lse1)
+
+
 def test_fp8_rejects_bad_arguments():
     q8 = torch.zeros((1, 1, 128, 64), dtype=torch.uint8, device="cuda")
     o = torch.empty((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")

@@ -81,6 +81,34 @@ def test_key_padding_zero_length():
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_long_runs_of_empty_units(d):
+    """Key lengths 0 for all batch rows but the last, with several work units per
+    CTA: each CTA meets runs of units without any key tile (epilogues that wait
+    for no product) before the last batch row's real ones. Empty rows give O = 0
+    and lse = -inf; the last row equals the same kernel run on it alone (bit for
+    bit: a row's result does not depend on which CTA computes it) and the oracle."""
+    B, H, N = 16, 16, 1024
+    x = make_case(B, H, N, d, seed=21, with_grad=False)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    sl = torch.zeros(B, dtype=torch.int32)
+    sl[-1] = N - 3
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd(q, k, v, scale, seqlens_k=sl.cuda())
+    o1, lse1 = fa.fwd(q[-1:].contiguous(), k[-1:].contiguous(), v[-1:].contiguous(), scale,
+                      seqlens_k=sl[-1:].cuda())
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    assert torch.all(o[:-1] == 0) and torch.all(torch.isneginf(lse[:-1]))
+    assert torch.equal(o[-1:], o1) and torch.equal(lse[-1:], lse1)
+    heads = [(B - 1, 0), (B - 1, H - 1)]
+    ro, rl = oracle.fwd(oracle_heads(x["q"], heads), oracle_heads(x["k"], heads),
+                        oracle_heads(x["v"], heads), scale, seqlens_k=sl.numpy(), heads=heads,
+                        H=H)
+    check(np.stack([o[b, h].float().cpu().numpy() for b, h in heads]),
+          np.stack([lse[b, h].cpu().numpy() for b, h in heads]), ro, rl)
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_butterfly_block_mask(d):
     check(*run_fwd(1, 2, 1024, d, mask="butterfly", seed=5))
 
