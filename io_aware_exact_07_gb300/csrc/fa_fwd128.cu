@@ -540,15 +540,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           // P = exp2(s*c - m_ref), summed (undropped) into l, dropout applied,
-          // packed to bf16. Each 64-key half is stored into P_g as soon as it is
-          // formed (the first store waits until the previous PV, which reads
-          // P_g, has completed), so the stores overlap the next half's
-          // exponentials.
+          // packed to bf16 and stored into P_g, which the previous PV reads.
           const uint64_t c2 = f2_pack(c_log2, c_log2);
           const uint64_t nm2 = f2_pack(-m_use, -m_use);
           uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums
           uint32_t pk[64];
           bool pv_ok = true;
+          bool stored0 = false;  // first half already in P_g
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -576,21 +574,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[half * 32 + q4 * 8 + (e >> 1)] = pp;
               }
             }
-            if (half == 0 && n_done > 0) {
-              if (!mbar_wait_warp(bars.pv_done[g], pv_cnt & 1, tmo, abort_flag)) {
-                pv_ok = false;
-                break;
-              }
-              ++pv_cnt;
-              tc_fence_after();
-            }
-            // 128-byte swizzle: 16-byte unit v of the row's 64-key half at v ^ (t & 7)
+            // 128-byte swizzle: 16-byte unit v of the row's 64-key half h at v ^ (t & 7)
+            auto store_half = [&](int h) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              st_shared_v4(
-                  (prow ^ static_cast<uint32_t>(v << 4)) + static_cast<uint32_t>(half * 16384),
-                  pk[half * 32 + 4 * v], pk[half * 32 + 4 * v + 1], pk[half * 32 + 4 * v + 2],
-                  pk[half * 32 + 4 * v + 3]);
+              for (int v = 0; v < 8; ++v)
+                st_shared_v4(
+                    (prow ^ static_cast<uint32_t>(v << 4)) + static_cast<uint32_t>(h * 16384),
+                    pk[h * 32 + 4 * v], pk[h * 32 + 4 * v + 1], pk[h * 32 + 4 * v + 2],
+                    pk[h * 32 + 4 * v + 3]);
+            };
+            if (half == 0) {
+              // The first half goes out now if the previous PV (which reads P_g)
+              // has already completed; otherwise the second half's exponentials
+              // come first and the wait moves to the end of the row.
+              // (The sliding-window and dropout instances always wait here: their
+              // extra per-row state makes the deferred path spill.)
+              constexpr bool kAlwaysWait = WIN || DROPOUT;
+              const bool ready =
+                  n_done == 0 || kAlwaysWait ||
+                  __all_sync(0xffffffffu, mbar_test_wait(bars.pv_done[g], pv_cnt & 1));
+              if (ready) {
+                if (n_done > 0) {
+                  if (kAlwaysWait &&
+                      !mbar_wait_warp(bars.pv_done[g], pv_cnt & 1, tmo, abort_flag)) {
+                    pv_ok = false;
+                    break;
+                  }
+                  ++pv_cnt;
+                  tc_fence_after();
+                }
+                store_half(0);
+                stored0 = true;
+              }
+            } else {
+              if (!stored0) {
+                if (!mbar_wait_warp(bars.pv_done[g], pv_cnt & 1, tmo, abort_flag)) {
+                  pv_ok = false;
+                  break;
+                }
+                ++pv_cnt;
+                tc_fence_after();
+                store_half(0);
+              }
+              store_half(1);
+            }
           }
           if (!pv_ok) {
             fail();
