@@ -14,8 +14,9 @@ from _parity import GRAD_RTOL, make_case, oracle_heads, rel_fro
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_wait_times_out_and_context_survives():
-    x = make_case(1, 2, 512, 64, with_grad=False)
+@pytest.mark.parametrize("d", [64, 128])  # the two forward kernels
+def test_stalled_wait_times_out_and_context_survives(d):
+    x = make_case(1, 2, 512, d, with_grad=False)
     q, k, v = (t.cuda() for t in (x["q"], x["k"], x["v"]))
     fa.fa_device_status(clear=True)
     fa.fa_set_wait_timeout_ns(200_000_000)  # 0.2 s
@@ -32,7 +33,7 @@ def test_stalled_wait_times_out_and_context_survives():
     assert fa.fa_device_status(clear=True) == fa.FA_OK
     heads = [(0, 0), (0, 1)]
     ro, _ = oracle.fwd(oracle_heads(x["q"], heads), oracle_heads(x["k"], heads),
-                       oracle_heads(x["v"], heads), 1 / math.sqrt(64), heads=heads, H=2)
+                       oracle_heads(x["v"], heads), 1 / math.sqrt(d), heads=heads, H=2)
     got = np.stack([o[0, h].float().cpu().numpy() for h in range(2)])
     assert np.abs(got - ro).max() <= 1e-2
 
