@@ -21,6 +21,7 @@ sees, Q, O, lse) against the measured copy bandwidth.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -143,14 +144,21 @@ def ncu_traffic(kernel: str, workload: str):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks and throttle reasons while running.
+
+    The sampler starts `lead_s` before the timed region so that it is already
+    producing samples when the region begins (nvidia-smi takes a while to start),
+    and only the samples whose timestamps fall inside the region are summarised
+    (all of them if none does, e.g. for a region shorter than the interval)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, lead_s: float = 0.3):
         self.index = index
+        self.lead_s = lead_s
         self.proc = None
+        self.t_begin = self.t_end = None
 
     def __enter__(self):
         try:
@@ -158,11 +166,14 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(self.lead_s)
         except Exception:
             self.proc = None
+        self.t_begin = datetime.datetime.now()
         return self
 
     def __exit__(self, *a):
+        self.t_end = datetime.datetime.now()
         self.lines = []
         if self.proc is not None:
             self.proc.terminate()
@@ -174,24 +185,32 @@ class ClockSampler:
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        rows = []
         for ln in getattr(self, "lines", []):
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None
+            try:
+                sm, mx = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+            rows.append((ts, sm, mx, [n for n, v in zip(names, f[6:10]) if v.lower() == "active"]))
+        inside = [r for r in rows if r[0] is not None and self.t_begin is not None
+                  and self.t_begin <= r[0] <= self.t_end]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "whole sampler run (no sample inside the timed region)"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = sorted({n for r in inside for n in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
 
 
 # -------------------------------------------------------------------- our arm
