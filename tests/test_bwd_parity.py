@@ -99,6 +99,37 @@ def test_key_padding_many_units_every_head():
     check(got, ref[:3])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_long_runs_of_empty_units(d):
+    """Backward with key length 0 for all batch rows but the last, several work
+    units per CTA and most of them without any key: the empty rows' gradients are
+    zero, and the last row equals the same kernels run on it alone (bit for bit:
+    without dropout a row's result does not depend on which CTA computes it) and
+    the oracle."""
+    B, H, N = 16, 16, 1024
+    x = make_case(B, H, N, d, seed=23, with_grad=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    sl = torch.zeros(B, dtype=torch.int32)
+    sl[-1] = N - 7
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd(q, k, v, scale, seqlens_k=sl.cuda())
+    grads = fa.bwd(q, k, v, o, do, lse, scale, seqlens_k=sl.cuda())
+    one = lambda t: t[-1:].contiguous()
+    o1, l1 = fa.fwd(one(q), one(k), one(v), scale, seqlens_k=sl[-1:].cuda())
+    grads1 = fa.bwd(one(q), one(k), one(v), o1, one(do), l1, scale, seqlens_k=sl[-1:].cuda())
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    for name, g, g1 in zip(("dQ", "dK", "dV"), grads, grads1):
+        assert torch.all(g[:-1] == 0), f"{name}: nonzero gradient in a row without keys"
+        assert torch.equal(g[-1:], g1), f"{name}: last row differs from the single-row run"
+    heads = [(B - 1, 0), (B - 1, H - 1)]
+    ref = oracle.bwd(oracle_heads(x["q"], heads), oracle_heads(x["k"], heads),
+                     oracle_heads(x["v"], heads), oracle_heads(x["do"], heads), scale,
+                     seqlens_k=sl.numpy(), heads=heads, H=H)
+    got = [np.stack([t[b, h].float().cpu().numpy() for b, h in heads]) for t in grads]
+    check(got, ref[:3])
+
+
 def test_random_block_mask_with_empty_rows_and_columns():
     nb = 5
     g = np.random.default_rng(1)
