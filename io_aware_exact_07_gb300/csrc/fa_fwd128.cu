@@ -691,8 +691,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float w0 = a0 * inv, w1 = a1 * inv;
       const bool row_ok = row < N;
       // This warpgroup writes output columns [64 g, 64 g + 64) from both O_0 and O_1.
+      // Each warp first puts its 32 rows x 128 bytes into shared memory (the rows of
+      // P_g this warp itself writes, free once its last PV has completed), then
+      // stores them so that every instruction covers four whole 128-byte lines,
+      // eight lanes per row, instead of 32 rows with 16 bytes each. (The
+      // sliding-window instance stores its rows directly: the staging makes it
+      // spill.)
+      constexpr bool kStaged = !WIN;
       __nv_bfloat16* orow =
           args.o + (static_cast<size_t>(uc.bh) * N + static_cast<size_t>(row)) * kD + 64 * g;
+      const uint32_t stage = sP + static_cast<uint32_t>(g * L::kTileBytes + quad * 4096);
+      const uint32_t srow = stage + static_cast<uint32_t>(lane * 128);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {  // 16 columns at a time (fewer live registers)
         const uint32_t col = 64u * static_cast<uint32_t>(g) + 16u * static_cast<uint32_t>(c);
@@ -714,10 +723,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           pk[k] = pack_bf16x2(v0, v1);
         }
-        if (row_ok) {
+        if constexpr (kStaged) {
+          // 16-byte units 2 c and 2 c + 1 of the row, swizzled by the row (no bank
+          // conflicts)
+          st_shared_v4(srow + static_cast<uint32_t>(((2 * c) ^ (lane & 7)) << 4), pk[0], pk[1],
+                       pk[2], pk[3]);
+          st_shared_v4(srow + static_cast<uint32_t>(((2 * c + 1) ^ (lane & 7)) << 4), pk[4], pk[5],
+                       pk[6], pk[7]);
+        } else if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
           dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      if constexpr (kStaged) {
+        __syncwarp();
+        const int u = lane & 7;  // 16-byte unit of the row this lane stores
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3);  // row within the warp's 32
+          const uint4 val = ld_shared_v4(stage + static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4)));
+          const int orow_i = uc.qt * kTile + quad * 32 + r;
+          if (orow_i < N)
+            *reinterpret_cast<uint4*>(args.o +
+                                      (static_cast<size_t>(uc.bh) * N + static_cast<size_t>(orow_i)) *
+                                          kD +
+                                      64 * g + 8 * u) = val;
         }
       }
       if (row_ok && g == 0) {
