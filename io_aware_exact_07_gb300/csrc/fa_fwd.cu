@@ -69,7 +69,9 @@ struct FwdLayout {
   //           s_full[2], p_full[2], o_free[2], s_free[2], pv_done[2], drain, drain2, stall
   static constexpr int kNumBars = 2 + 1 + 4 * kStages + 10 + 3;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + slack for 1024-byte alignment
+  // epilogue staging: 4 KB per softmax warp (its 32 rows of O, 128 bytes each)
+  static constexpr int kStageOff = (kMiscOff + 64 + 127) / 128 * 128;
+  static constexpr int kSmemBytes = kStageOff + 8 * 4096 + 1024;  // + slack for 1024-byte alignment
   // Tensor memory has room for a separate P buffer per query tile
   // (2 x (128 S + 64 P + 64 O) = 512 columns), so the next S can be computed
   // while the softmax still works on the current one.
@@ -683,8 +685,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       const bool row_ok = row < N;
       const float inv = (l_sum > 0.f) ? args.drop.keep_scale / l_sum : 0.f;
-      __nv_bfloat16* orow =
-          args.o + (static_cast<size_t>(uc.bh) * N + static_cast<size_t>(row)) * D;
+      // The warp puts its 32 rows x 128 bytes of O into its own staging area, then
+      // stores them so that every instruction covers four whole 128-byte lines,
+      // eight lanes per row, instead of 32 rows with 16 bytes each.
+      const uint32_t stage = smem_u32(smem + L::kStageOff) + static_cast<uint32_t>(warp * 4096);
+      const uint32_t srow = stage + static_cast<uint32_t>(lane * 128);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -699,11 +704,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           pk[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        for (int k = 0; k < 4; ++k)  // 16-byte unit 4 c + k, swizzled by the row
+          st_shared_v4(srow + static_cast<uint32_t>(((4 * c + k) ^ (lane & 7)) << 4), pk[4 * k],
+                       pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+      }
+      __syncwarp();
+      {
+        const int u = lane & 7;  // 16-byte unit of the row this lane stores
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3);  // row within the warp's 32
+          const uint4 val = ld_shared_v4(stage + static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4)));
+          const int orow_i = qt * kTile + quad * 32 + r;
+          if (orow_i < N)
+            *reinterpret_cast<uint4*>(
+                args.o + (static_cast<size_t>(uc.bh) * N + static_cast<size_t>(orow_i)) * D + 8 * u) =
+                val;
         }
       }
       if (row_ok) {
