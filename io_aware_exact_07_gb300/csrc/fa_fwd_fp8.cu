@@ -588,27 +588,48 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       const bool row_ok = row < N;
       const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
       const float* sv = args.s_v + static_cast<size_t>(uc.bhk) * 128;
-      __nv_bfloat16* orow = args.o + (static_cast<size_t>(uc.bh) * N + static_cast<size_t>(row)) * 128;
+      // O goes out 64 columns at a time: the warp puts its 32 rows x 128 bytes into
+      // the rows of P_x it writes itself (free once its last PV has completed), then
+      // stores them so that every instruction covers four whole 128-byte lines,
+      // eight lanes per row, instead of 32 rows with 16 bytes each.
+      const uint32_t stage = sP + static_cast<uint32_t>(x * L::kTileBytes + quad * 4096);
+      const uint32_t srow = stage + static_cast<uint32_t>(lane * 128);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        if (n_done > 0) {
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-        } else {
+      for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = 0u;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * h + cc;
+          uint32_t o[32];
+          if (n_done > 0) {
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv * sv[c * 32 + 2 * k],
+                               __uint_as_float(o[2 * k + 1]) * inv * sv[c * 32 + 2 * k + 1]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)  // 16-byte unit 4 cc + k, swizzled by the row
+            st_shared_v4(srow + static_cast<uint32_t>(((4 * cc + k) ^ (lane & 7)) << 4), w[4 * k],
+                         w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
         }
-        uint32_t w[16];
+        __syncwarp();
+        const int u = lane & 7;  // 16-byte unit of the row this lane stores
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv * sv[c * 32 + 2 * k],
-                             __uint_as_float(o[2 * k + 1]) * inv * sv[c * 32 + 2 * k + 1]);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3);  // row within the warp's 32
+          const uint4 val = ld_shared_v4(stage + static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4)));
+          const int orow_i = (uc.qt0 + x) * kTile + quad * 32 + r;
+          if (orow_i < N)
+            *reinterpret_cast<uint4*>(
+                args.o + (static_cast<size_t>(uc.bh) * N + static_cast<size_t>(orow_i)) * 128 +
+                64 * h + 8 * u) = val;
         }
+        __syncwarp();  // the staging rows are written again by the next half
       }
       if (row_ok)
         args.lse[static_cast<size_t>(uc.bh) * N + row] =
