@@ -66,7 +66,8 @@ struct Layout {
   //           s_full[2], s_free[2], p_full[2], pv_done[2], o_free, xbar[4],
   //           drain, drain2, stall
   static constexpr int kNumBars = 26;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // abort flag, tensor-memory address
+  // abort flag, tensor-memory address, units whose PVs are all issued
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kXchOff = kMiscOff + 16;            // (m, l) per warpgroup and row
   // No alignment slack: the kernel checks that the dynamic shared memory starts
   // on a 1024-byte boundary, which the swizzled tiles need.
@@ -134,6 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff + 8);
+  // units (in this CTA's order) whose PVs have all been issued: a count, not a
+  // barrier phase, since the PV issuer may run several units without key tiles
+  // ahead of the S issuer
+  volatile int* pv_units = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
   Bars bars;
   {
@@ -181,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (units without key tiles would otherwise let the epilogues run ahead).
     mbar_init(bars.o_free, 257);
     for (int q = 0; q < 4; ++q) mbar_init(bars.xbar[q], 64);
+    *pv_units = 0;
     mbar_init(bars.drain, 1);
     mbar_init(bars.drain2, 1);
     mbar_init(bars.stall, 1);
@@ -298,9 +304,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit uc = decode_unit(u, mk.H, n_q, mk.causal);
         const int n_kv = (kv_len_of(mk, uc.b) + kTile - 1) / kTile;
         const int jmax = key_tile_bound(mk, uc.qt, n_kv);
-        if (leader && !mbar_wait(bars.q_full, unit_count & 1, tmo, abort_flag)) {
-          fail();
-          ok = false;
+        // The tensor core runs products in issue order: the next unit's S products
+        // wait until the PV issuer has issued this unit's last PV, so that they
+        // do not delay it (the softmax warpgroups' epilogue waits for that PV; they
+        // need the next S only after the epilogue).
+        if (leader) {
+          bool ready = *pv_units >= unit_count;
+          if (!ready) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!(ready = *pv_units >= unit_count)) {
+              if (*abort_flag || globaltimer_ns() - t0 > tmo) break;
+              __nanosleep(64);  // leave issue slots to the softmax warps meanwhile
+            }
+          }
+          if (!ready || !mbar_wait(bars.q_full, unit_count & 1, tmo, abort_flag)) {
+            fail();
+            ok = false;
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         int pos = 0;  // position in the unit's tile list
@@ -436,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(bars.o_free);
           }
         }
+        if (leader && ok) *pv_units = unit_count + 1;  // this unit's PVs are all issued
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (leader) {
