@@ -301,9 +301,10 @@ fa_status fa_butterfly_mask(uint8_t* mask_host, int nb);
 /* Reads the status word of the current device after synchronising `stream`;
  * returns FA_OK or the first device-side error recorded since the last clear:
  * FA_ERR_TIMEOUT (a bounded wait ran out), or FA_ERR_CUDA when a kernel found
- * its launch unusable and returned without work (the d = 128 key-tile backward
- * kernel uses all 227 KB of shared memory with no alignment slack and checks
- * that its dynamic shared memory starts on a 1024-byte boundary).
+ * its launch unusable and returned without work (the d = 128 forward and the
+ * d = 128 key-tile backward kernel use nearly all 227 KB of shared memory with
+ * no alignment slack and check that their dynamic shared memory starts on a
+ * 1024-byte boundary).
  * clear != 0 resets it to FA_OK.
  * The word is one per device, shared by every call on that device: the
  * forward entry points take no workspace to hold a per-call word. An error
