@@ -684,7 +684,12 @@ struct DqL {
   static constexpr int kBarOff = kVOff + kVStages * T;
   static constexpr int kNumBars = 4 + 2 * kMaxKStages + 2 * kMaxVStages + 11;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+  // d = 64: the epilogue stages each compute warp's 32 rows of dQ (1 KB) before
+  // storing them coalesced; at d = 128 shared memory has no room for it.
+  static constexpr bool kStageDq = (D == 64);
+  static constexpr int kStageOff = (kMiscOff + 64 + 127) / 128 * 128;
+  static constexpr int kSmemBytes = kStageOff + (kStageDq ? kComputeWarps * 1024 : 0) + 1024;
+  static_assert(kSmemBytes <= 232448, "dQ layout exceeds 227 KB of shared memory");
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
 };
 
@@ -1191,7 +1196,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < kQCols / 2; ++k)
         o[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * args.scale,
                            __uint_as_float(v[2 * k + 1]) * args.scale);
-      if (row_in) {
+      if constexpr (L::kStageDq) {
+        // The warp's 32 rows x 32 bytes go through shared memory so that each
+        // store instruction writes 16 rows' whole 32-byte segments instead of 32
+        // half segments. Row r's two 16-byte units swap places on rows 4-7 of
+        // every 8 (no bank conflicts either way).
+        const uint32_t stage = smem_u32(smem + L::kStageOff) + static_cast<uint32_t>(warp * 1024);
+        const uint32_t sw = static_cast<uint32_t>(lane >> 2) & 1u;
+        st_shared_v4(stage + static_cast<uint32_t>(lane * 32) + (sw << 4), o[0], o[1], o[2], o[3]);
+        st_shared_v4(stage + static_cast<uint32_t>(lane * 32) + ((sw ^ 1u) << 4), o[4], o[5], o[6],
+                     o[7]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = 16 * i + (lane >> 1);  // row within the warp's 32
+          const uint32_t u = static_cast<uint32_t>(lane & 1);
+          const uint4 val = ld_shared_v4(stage + static_cast<uint32_t>(r * 32) +
+                                         ((u ^ (static_cast<uint32_t>(r >> 2) & 1u)) << 4));
+          const int row_r = qt * kTile + quad * 32 + r;
+          if (row_r < N)
+            *reinterpret_cast<uint4*>(args.dq +
+                                      (static_cast<size_t>(bh) * N + static_cast<size_t>(row_r)) * D +
+                                      kQCols * wg + 8 * u) = val;
+        }
+      } else if (row_in) {
         uint4* d4 = reinterpret_cast<uint4*>(args.dq + static_cast<size_t>(ridx) * D + kQCols * wg);
 #pragma unroll
         for (int k = 0; k < kQCols / 8; ++k)
