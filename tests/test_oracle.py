@@ -157,7 +157,11 @@ def test_fully_masked_row_is_zero():
 def _torch_sdpa(q, k, v, scale, mask):
     qt, kt, vt = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
     m = torch.tensor(mask)
-    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m, scale=scale)
+    # the math backend: softmax(scale Q K^T + mask) V as plain tensor ops, the same
+    # on every run (a blocked CPU kernel could otherwise be picked)
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    with sdpa_kernel(SDPBackend.MATH):
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m, scale=scale)
     return qt, kt, vt, o
 
 
